@@ -1,0 +1,305 @@
+// attn_api.cu -- the C ABI (include/attn.h): argument validation, TMA tensor-map encoding,
+// the per-device status word and dispatch to the kernels.  Nothing here allocates device
+// memory; every launch goes on the caller's stream.
+#include <cudaTypedefs.h>
+#include <cmath>
+#include <cstdint>
+#include <initializer_list>
+#include <mutex>
+#include "kernels.h"
+
+namespace {
+
+using attn::BwdMaps;
+using attn::BwdParams;
+using attn::FwdMaps;
+using attn::FwdParams;
+
+// First error recorded by a kernel on this device (0 = none); cleared by attn_get_device_status.
+__device__ unsigned g_attn_status;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+unsigned* status_word() {
+  static std::mutex mu;
+  static unsigned* cache[256] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_attn_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned*>(ptr);
+  }
+  return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// 128-byte-swizzled tile map with a {64 elements, rows} box over the innermost (head_dim) and
+// the row dimension.  rank 3 = dense {d, N, B*H}; rank 4 = packed varlen {d, H, 3, T}.
+bool make_map(CUtensorMap* map, const void* base, attn_dtype_t dt, int rank, const uint64_t* dims,
+              const uint64_t* strides_bytes, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t =
+      dt == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = fn(map, t, rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_dense_map(CUtensorMap* map, const void* base, attn_dtype_t dt, int heads_total, int N, int d) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(N), static_cast<uint64_t>(heads_total)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(N) * d * 2};
+  const uint32_t box[3] = {64, 128, 1};
+  return make_map(map, base, dt, 3, dims, strides, box);
+}
+
+bool make_packed_map(CUtensorMap* map, const void* base, attn_dtype_t dt, int T, int H, int d) {
+  const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(H), 3, static_cast<uint64_t>(T)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(H) * d * 2,
+                               3ull * H * d * 2};
+  const uint32_t box[4] = {64, 1, 1, 128};
+  return make_map(map, base, dt, 4, dims, strides, box);
+}
+
+attn_status_t check_common(int d, float scale, attn_dtype_t dt) {
+  if (dt != ATTN_F32 && dt != ATTN_F16 && dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (!(scale >= 0.f) || std::isinf(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (d % 16 != 0 || d > 128) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+float resolve_scale(float scale, int d) { return scale == 0.f ? 1.f / std::sqrt(static_cast<float>(d)) : scale; }
+
+attn_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int N, int d, int causal, float scale, attn_dtype_t dtype, unsigned flags, void* stream) {
+  attn_status_t st = check_common(d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAG_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  const bool f32 = dtype == ATTN_F32;
+  const int rows_per_tile = f32 ? 32 : attn::kBM;
+  const int n_qtiles = (N + rows_per_tile - 1) / rows_per_tile;
+  if (n_qtiles > 65535) return ATTN_ERR_UNSUPPORTED;
+
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.status = status_word();
+  if (!p.status) return ATTN_ERR_CUDA;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.G = Hq / Hkv;
+  p.n_qtiles = n_qtiles;
+  p.scale = resolve_scale(scale, d);
+  p.scale_log2 = p.scale * kLog2e;
+  p.out_f32 = (flags & ATTN_FLAG_OUT_F32) ? 1 : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (f32) return from_cuda(attn::launch_fwd_f32(q, k, v, p, causal != 0, false, s));
+  FwdMaps maps;
+  if (!make_dense_map(&maps.q, q, dtype, B * Hq, N, d) || !make_dense_map(&maps.k, k, dtype, B * Hkv, N, d) ||
+      !make_dense_map(&maps.v, v, dtype, B * Hkv, N, d))
+    return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_fwd_tc(maps, p, dtype, causal != 0, false, s));
+}
+
+attn_status_t attn_fwd_varlen(const void* qkv, const int32_t* cu_seqlens, int nseq, int total_tokens,
+                              int max_seqlen, void* out, float* lse, int H, int d, int causal, float scale,
+                              attn_dtype_t dtype, unsigned flags, void* stream) {
+  attn_status_t st = check_common(d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (nseq < 0 || total_tokens < 0 || max_seqlen < 0 || H <= 0) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAG_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (nseq == 0) return total_tokens == 0 ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+  if (!cu_seqlens || !aligned(cu_seqlens, 4)) return ATTN_ERR_INVALID_ARG;
+  if (total_tokens == 0) return ATTN_OK;  // every sequence is empty
+  if (max_seqlen == 0) return ATTN_ERR_INVALID_ARG;
+  if (!qkv || !out || !aligned(qkv, 16) || !aligned(out, 16) || !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+  if (nseq > 65535) return ATTN_ERR_UNSUPPORTED;
+  const bool f32 = dtype == ATTN_F32;
+  const int rows_per_tile = f32 ? 32 : attn::kBM;
+  const int n_qtiles = (max_seqlen + rows_per_tile - 1) / rows_per_tile;
+  if (n_qtiles > 65535) return ATTN_ERR_UNSUPPORTED;
+
+  FwdParams p{};
+  p.o = out;
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.status = status_word();
+  if (!p.status) return ATTN_ERR_CUDA;
+  p.B = 1; p.Hq = H; p.Hkv = H; p.N = 0; p.d = d; p.G = 1;
+  p.nseq = nseq; p.total_tokens = total_tokens; p.max_seqlen = max_seqlen;
+  p.n_qtiles = n_qtiles;
+  p.scale = resolve_scale(scale, d);
+  p.scale_log2 = p.scale * kLog2e;
+  p.out_f32 = (flags & ATTN_FLAG_OUT_F32) ? 1 : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t plane = static_cast<size_t>(H) * d;
+  if (f32) {
+    const float* base = static_cast<const float*>(qkv);
+    return from_cuda(attn::launch_fwd_f32(base, base + plane, base + 2 * plane, p, causal != 0, true, s));
+  }
+  FwdMaps maps;
+  if (!make_packed_map(&maps.q, qkv, dtype, total_tokens, H, d)) return ATTN_ERR_CUDA;
+  maps.k = maps.q;
+  maps.v = maps.q;
+  return from_cuda(attn::launch_fwd_tc(maps, p, dtype, causal != 0, true, s));
+}
+
+size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int d) {
+  if (B <= 0 || Hq <= 0 || N <= 0 || d <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * N;
+  return round256(rows * d * sizeof(float)) + round256(rows * sizeof(float));
+}
+
+namespace {
+
+// Shared validation of the backward's sizes and workspace; fills the common BwdParams fields.
+attn_status_t bwd_setup(BwdParams* p, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
+                        float scale, attn_dtype_t dtype, unsigned flags) {
+  attn_status_t st = check_common(d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAG_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return ATTN_OK;
+  if (!workspace || !aligned(workspace, 256)) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, N, d)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if ((N + 31) / 32 > 65535) return ATTN_ERR_UNSUPPORTED;
+  const size_t rows = static_cast<size_t>(B) * Hq * N;
+  p->dq_acc = static_cast<float*>(workspace);
+  p->delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * d * sizeof(float)));
+  p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->N = N; p->d = d; p->G = Hq / Hkv;
+  p->n_ktiles = (N + attn::kBN - 1) / attn::kBN;
+  p->scale = resolve_scale(scale, d);
+  p->scale_log2 = p->scale * kLog2e;
+  p->out_f32 = (flags & ATTN_FLAG_OUT_F32) ? 1 : 0;
+  return ATTN_OK;
+}
+
+bool all_aligned16(std::initializer_list<const void*> ptrs) {
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned(ptr, 16)) return false;
+  return true;
+}
+
+}  // namespace
+
+attn_status_t attn_bwd_prepare(const void* o, const void* dout, void* workspace, size_t workspace_bytes, int B,
+                               int Hq, int N, int d, attn_dtype_t dtype, void* stream) {
+  BwdParams p{};
+  attn_status_t st = bwd_setup(&p, workspace, workspace_bytes, B, Hq, Hq, N, d, 0.f, dtype, 0);
+  if (st != ATTN_OK || B == 0 || N == 0) return st;
+  if (!all_aligned16({o, dout})) return ATTN_ERR_INVALID_ARG;
+  p.o = o;
+  p.dout = dout;
+  if (!(p.status = status_word())) return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_bwd_preprocess(p, dtype, dtype != ATTN_F32, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse, void* dq,
+                            void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                            int N, int d, int causal, float scale, attn_dtype_t dtype, unsigned flags,
+                            void* stream) {
+  BwdParams p{};
+  attn_status_t st = bwd_setup(&p, workspace, workspace_bytes, B, Hq, Hkv, N, d, scale, dtype, flags);
+  if (st != ATTN_OK || B == 0 || N == 0) return st;
+  if (!all_aligned16({q, k, v, dout, dk, dv}) || !lse || !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+  if (dtype == ATTN_F32 && !all_aligned16({dq})) return ATTN_ERR_INVALID_ARG;
+  p.q = q; p.k = k; p.v = v; p.dout = dout; p.lse = lse;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  if (!(p.status = status_word())) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_F32) return from_cuda(attn::launch_bwd_f32(p, causal != 0, s));
+  BwdMaps maps;
+  if (!make_dense_map(&maps.q, q, dtype, B * Hq, N, d) || !make_dense_map(&maps.k, k, dtype, B * Hkv, N, d) ||
+      !make_dense_map(&maps.v, v, dtype, B * Hkv, N, d) || !make_dense_map(&maps.dout, dout, dtype, B * Hq, N, d))
+    return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_bwd_tc(maps, p, dtype, causal != 0, s));
+}
+
+attn_status_t attn_bwd_finish(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int N, int d,
+                              float scale, attn_dtype_t dtype, unsigned flags, void* stream) {
+  BwdParams p{};
+  attn_status_t st = bwd_setup(&p, workspace, workspace_bytes, B, Hq, Hq, N, d, scale, dtype, flags);
+  if (st != ATTN_OK || B == 0 || N == 0) return st;
+  if (dtype == ATTN_F32) return ATTN_OK;  // the fp32 main step wrote dq itself
+  if (!all_aligned16({dq})) return ATTN_ERR_INVALID_ARG;
+  p.dq = dq;
+  if (!(p.status = status_word())) return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_bwd_postprocess(p, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                       void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                       int N, int d, int causal, float scale, attn_dtype_t dtype, unsigned flags, void* stream) {
+  BwdParams p{};
+  attn_status_t st = bwd_setup(&p, workspace, workspace_bytes, B, Hq, Hkv, N, d, scale, dtype, flags);
+  if (st != ATTN_OK || B == 0 || N == 0) return st;
+  if (!all_aligned16({q, k, v, o, dout, dq, dk, dv}) || !lse || !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+  st = attn_bwd_prepare(o, dout, workspace, workspace_bytes, B, Hq, N, d, dtype, stream);
+  if (st == ATTN_OK)
+    st = attn_bwd_main(q, k, v, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, causal, scale,
+                       dtype, flags, stream);
+  if (st == ATTN_OK) st = attn_bwd_finish(dq, workspace, workspace_bytes, B, Hq, N, d, scale, dtype, flags, stream);
+  return st;
+}
+
+attn_status_t attn_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned* w = status_word();
+  if (!w) return ATTN_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return static_cast<attn_status_t>(v);
+}
+
+const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case ATTN_ERR_DEVICE_INPUT: return "invalid cu_seqlens / max_seqlen detected on the device";
+  }
+  return "unknown status";
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,357 @@
+// bwd_tc.cuh -- tcgen05 backward for fp16 / bf16 (dQ, dK, dV), KV-stationary.
+//
+// The backward recomputes the scores from Q, K and the forward's LSE instead of storing them
+// (FlashAttention-T review, FAQ 4; best practice 2 on keeping the backward fused).  With
+// P_ij = exp(S_ij - LSE_i), dP_ij = dO_i . V_j, D_i = dO_i . O_i and dS_ij = P_ij (dP_ij - D_i):
+//   dV_j = sum_i P_ij dO_i,   dK_j = scale sum_i dS_ij Q_i,   dQ_i = scale sum_j dS_ij K_j,
+// where i runs over every query row of every query head of the kv head's GQA group.
+//
+// One CTA owns one 128-key tile of one (batch, kv head): K and V stay in shared memory, and
+// the CTA walks (query head of the group) x (query tile at or after the key tile when causal).
+// Per query tile, in TMEM (lane = key for the first four, lane = query for dQ):
+//   S^T  = K Q^T      (128 x 128 fp32)       dP^T = V dO^T   (128 x 128 fp32)
+//   dV  += P^T dO     (128 x d, over all iterations)
+//   dK  += dS^T Q     (128 x d, over all iterations)
+//   dQ_t = dS K       (128 x d; reduced into the fp32 workspace with vector atomics)
+// Warps 0-3 turn S^T / dP^T into P^T and dS^T (16-bit, 128-byte swizzled, K-major) in shared
+// memory, then move dQ_t out of TMEM into the workspace; at the end they write dK and dV.
+// Warp 4 is the TMA producer (and TMEM allocator), warp 5 issues the MMAs.
+// The same shared-memory tile serves as a K-major operand in one MMA and as an MN-major
+// operand in another (Q, dO, K, and dS^T read as dS).
+#pragma once
+#include "fwd_tc.cuh"
+
+namespace attn {
+
+template <int DP>
+struct BwdLayout {
+  static constexpr int kQStages = DP == 128 ? 1 : 2;
+  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kTileBytes = (DP / 64) * kChunkBytes;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffQ = kOffV + kTileBytes;                 // kQStages tiles
+  static constexpr int kOffdO = kOffQ + kQStages * kTileBytes;     // kQStages tiles
+  static constexpr int kOffP = kOffdO + kQStages * kTileBytes;     // P^T  [128 keys x 128 queries]
+  static constexpr int kOffdS = kOffP + 2 * kChunkBytes;           // dS^T [128 keys x 128 queries]
+  static constexpr int kOffRow = kOffdS + 2 * kChunkBytes;         // LSE*log2e and D, 2 buffers each
+  static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
+  // kv_full, q_full[QS], q_empty[QS], sdp_full, ds_full, dq_full, dq_free, dkdv_done, drain,
+  // rows_ready
+  static constexpr int kNumBars = 1 + 2 * kQStages + 7;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kSmemAlloc = kBytes + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns
+  static constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 256 + DP;
+  static constexpr uint32_t kColdQ = DP == 128 ? 0 : 384;  // d = 128: dQ reuses the S^T columns
+};
+
+template <typename T, int DP, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const BwdParams p) {
+  using L = BwdLayout<DP>;
+  constexpr int QS = L::kQStages;
+  constexpr int kChunks = DP / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sK = smem + L::kOffK;
+  uint8_t* sV = smem + L::kOffV;
+  uint8_t* sQ = smem + L::kOffQ;
+  uint8_t* sdO = smem + L::kOffdO;
+  uint8_t* sP = smem + L::kOffP;
+  uint8_t* sdS = smem + L::kOffdS;
+  float* sLse = reinterpret_cast<float*>(smem + L::kOffRow);  // [2][128]
+  float* sD = sLse + 256;                                       // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + QS;
+  uint64_t* sdp_full = q_empty + QS;
+  uint64_t* ds_full = sdp_full + 1;
+  uint64_t* dq_full = ds_full + 1;
+  uint64_t* dq_free = dq_full + 1;
+  uint64_t* dkdv_done = dq_free + 1;
+  uint64_t* drain = dkdv_done + 1;
+  uint64_t* rows_ready = drain + 1;  // the 128 row terms (LSE, D) of the current tile are in smem
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kt = blockIdx.x;  // key tile; 0 first = the heaviest under the causal mask
+  const int b = blockIdx.y / p.Hkv, g = blockIdx.y % p.Hkv;
+  const int N = p.N;
+  const int n_q = (N + kBM - 1) / kBM;
+  const int qt0 = CAUSAL ? kt : 0;
+  const int per_head = n_q - qt0;
+  const int n_it = p.G * per_head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < QS; ++i) {
+      mbar_init(q_full + i, 1);
+      mbar_init(q_empty + i, 1);
+    }
+    mbar_init(sdp_full, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(dkdv_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(rows_ready, 128);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 4) tmem_alloc(tmem_slot, L::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_expect_tx(kv_full, 2 * L::kTileBytes);
+      for (int c = 0; c < kChunks; ++c) {
+        tma_load_3d(sK + c * L::kChunkBytes, &tmK, kv_full, c * 64, kt * kBN, b * p.Hkv + g);
+        tma_load_3d(sV + c * L::kChunkBytes, &tmV, kv_full, c * 64, kt * kBN, b * p.Hkv + g);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int h = g * p.G + it / per_head, qt = qt0 + it % per_head;
+        const int st = it % QS;
+        if (it >= QS && !mbar_wait(q_empty + st, ((it / QS) - 1) & 1, abort_flag, p.status)) break;
+        mbar_expect_tx(q_full + st, 2 * L::kTileBytes);
+        for (int c = 0; c < kChunks; ++c) {
+          tma_load_3d(sQ + st * L::kTileBytes + c * L::kChunkBytes, &tmQ, q_full + st, c * 64, qt * kBM,
+                      b * p.Hq + h);
+          tma_load_3d(sdO + st * L::kTileBytes + c * L::kChunkBytes, &tmdO, q_full + st, c * 64, qt * kBM,
+                      b * p.Hq + h);
+        }
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        mbar_drain(kv_full, 0);
+        for (int it = max(0, issued - QS); it < issued; ++it) mbar_drain(q_full + it % QS, (it / QS) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr bool kB = Elem<T>::kBf16;
+      constexpr uint32_t idSS = idesc_f16(kB, false, false, 128, 128);  // S^T, dP^T
+      constexpr uint32_t idKD = idesc_f16(kB, false, true, 128, DP);    // dV, dK: B MN-major
+      constexpr uint32_t idQ = idesc_f16(kB, true, true, 128, DP);      // dQ: A and B MN-major
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
+      const uint32_t aP = smem_u32(sP), adS = smem_u32(sdS);
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % QS;
+        if (!mbar_wait(q_full + st, (it / QS) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (it >= 1 && !mbar_wait(dq_free, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qbase = aQ + st * L::kTileBytes, dobase = adO + st * L::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < DP / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * L::kChunkBytes + (ks & 3) * 32;
+          mma_ss(tmem + L::kColS, smem_desc_sw128(aK + off, 16, 1024), smem_desc_sw128(qbase + off, 16, 1024),
+                 idSS, ks > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int ks = 0; ks < DP / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * L::kChunkBytes + (ks & 3) * 32;
+          mma_ss(tmem + L::kColdP, smem_desc_sw128(aV + off, 16, 1024), smem_desc_sw128(dobase + off, 16, 1024),
+                 idSS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(sdp_full);
+        if (!mbar_wait(ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {  // reduction over the 128 queries of the tile
+          const uint32_t a_off = (ks >> 2) * L::kChunkBytes + (ks & 3) * 32;
+          mma_ss(tmem + L::kColdV, smem_desc_sw128(aP + a_off, 16, 1024),
+                 smem_desc_sw128(dobase + ks * 2048, L::kChunkBytes, 1024), idKD, (it > 0 || ks > 0) ? 1u : 0u);
+          mma_ss(tmem + L::kColdK, smem_desc_sw128(adS + a_off, 16, 1024),
+                 smem_desc_sw128(qbase + ks * 2048, L::kChunkBytes, 1024), idKD, (it > 0 || ks > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {  // reduction over the 128 keys of the tile
+          mma_ss(tmem + L::kColdQ, smem_desc_sw128(adS + ks * 2048, L::kChunkBytes, 1024),
+                 smem_desc_sw128(aK + ks * 2048, L::kChunkBytes, 1024), idQ, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(dq_full);
+        mma_commit(q_empty + st);
+      }
+      if (ok) {
+        mma_commit(dkdv_done);
+      } else {
+        mma_commit(drain);
+        mbar_drain(drain, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ warps 0-3
+    const int t = threadIdx.x;  // TMEM lane: key row of S^T/dP^T/dK/dV, query row of dQ
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int key = kt * kBN + t;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int h = g * p.G + it / per_head, qt = qt0 + it % per_head;
+      const size_t row_base = (static_cast<size_t>(b) * p.Hq + h) * N;
+      float* lse_buf = sLse + (it & 1) * 128;
+      float* d_buf = sD + (it & 1) * 128;
+      {
+        const int q = qt * kBM + t;
+        lse_buf[t] = q < N ? p.lse[row_base + q] * 1.4426950408889634f : INFINITY;
+        d_buf[t] = q < N ? p.delta[row_base + q] : 0.f;
+      }
+      mbar_arrive(rows_ready);
+      if (!mbar_wait(rows_ready, it & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!mbar_wait(sdp_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const bool key_ok = key < N;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t rs[32], rd[32];
+        tmem_ld32(tl + L::kColS + cc * 32, rs);
+        tmem_ld32(tl + L::kColdP + cc * 32, rd);
+        tmem_ld_wait();
+        tmem_reg_fence(rs);
+        tmem_reg_fence(rd);
+        float pv[32], dsv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int qi = cc * 32 + i;
+          const int q = qt * kBM + qi;
+          float pr = ex2_approx(fmaf(__uint_as_float(rs[i]), sl2, -lse_buf[qi]));
+          if (!key_ok || (CAUSAL && q < key)) pr = 0.f;
+          pv[i] = pr;
+          dsv[i] = pr * (__uint_as_float(rd[i]) - d_buf[qi]);
+        }
+        // 32 queries = 4 16-byte granules of this key's 256-byte P^T / dS^T row
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          const int gq = cc * 4 + gi;  // granule index over 128 queries
+          const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
+          uint4 a, c;
+          a.x = Elem<T>::pack(pv[gi * 8 + 0], pv[gi * 8 + 1]);
+          a.y = Elem<T>::pack(pv[gi * 8 + 2], pv[gi * 8 + 3]);
+          a.z = Elem<T>::pack(pv[gi * 8 + 4], pv[gi * 8 + 5]);
+          a.w = Elem<T>::pack(pv[gi * 8 + 6], pv[gi * 8 + 7]);
+          c.x = Elem<T>::pack(dsv[gi * 8 + 0], dsv[gi * 8 + 1]);
+          c.y = Elem<T>::pack(dsv[gi * 8 + 2], dsv[gi * 8 + 3]);
+          c.z = Elem<T>::pack(dsv[gi * 8 + 4], dsv[gi * 8 + 5]);
+          c.w = Elem<T>::pack(dsv[gi * 8 + 6], dsv[gi * 8 + 7]);
+          *reinterpret_cast<uint4*>(sP + off) = a;
+          *reinterpret_cast<uint4*>(sdS + off) = c;
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+      // dQ_t (lane = query row) -> fp32 workspace
+      if (!mbar_wait(dq_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const int q = qt * kBM + t;
+        float* dst = p.dq_acc + (row_base + q) * static_cast<size_t>(p.d);
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < DP / 32; ++c) {
+          tmem_ld32(tl + L::kColdQ + c * 32, r);
+          tmem_ld_wait();
+          tmem_reg_fence(r);
+          if (q < N && c * 32 < p.d) {
+            const int ncol = min(32, p.d - c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (i * 4 < ncol)
+                atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + i * 4),
+                          make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                      __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+    }
+    // ---- epilogue: dK (scaled) and dV rows of this key tile
+    if (ok && mbar_wait(dkdv_done, 0, abort_flag, p.status)) {
+      tc_fence_after();
+      const size_t krow = (static_cast<size_t>(b) * p.Hkv + g) * N + key;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? L::kColdK : L::kColdV;
+        const float mul = which == 0 ? p.scale : 1.f;
+        void* out = which == 0 ? p.dk : p.dv;
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < DP / 32; ++c) {
+          tmem_ld32(tl + col + c * 32, r);
+          tmem_ld_wait();
+          tmem_reg_fence(r);
+          if (key < N && c * 32 < p.d) {
+            const int ncol = min(32, p.d - c * 32);
+            if (p.out_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + krow * p.d + c * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (i * 4 < ncol)
+                  dst[i] = make_float4(__uint_as_float(r[4 * i]) * mul, __uint_as_float(r[4 * i + 1]) * mul,
+                                       __uint_as_float(r[4 * i + 2]) * mul, __uint_as_float(r[4 * i + 3]) * mul);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(out) + krow * p.d + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (i * 8 < ncol) {
+                  uint4 v;
+                  v.x = Elem<T>::pack(__uint_as_float(r[8 * i + 0]) * mul, __uint_as_float(r[8 * i + 1]) * mul);
+                  v.y = Elem<T>::pack(__uint_as_float(r[8 * i + 2]) * mul, __uint_as_float(r[8 * i + 3]) * mul);
+                  v.z = Elem<T>::pack(__uint_as_float(r[8 * i + 4]) * mul, __uint_as_float(r[8 * i + 5]) * mul);
+                  v.w = Elem<T>::pack(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul);
+                  dst[i] = v;
+                }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <typename T, int DP, bool CAUSAL>
+cudaError_t launch_bwd_tc_t(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream) {
+  using L = BwdLayout<DP>;
+  auto kern = bwd_tc_kernel<T, DP, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(p.n_ktiles, p.B * p.Hkv);
+  kern<<<grid, 192, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, maps.dout, p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_bwd_tc_dtype(const BwdMaps& maps, const BwdParams& p, bool causal, cudaStream_t stream) {
+  if (p.d <= 64)
+    return causal ? launch_bwd_tc_t<T, 64, true>(maps, p, stream) : launch_bwd_tc_t<T, 64, false>(maps, p, stream);
+  return causal ? launch_bwd_tc_t<T, 128, true>(maps, p, stream) : launch_bwd_tc_t<T, 128, false>(maps, p, stream);
+}
+
+}  // namespace attn

@@ -1,0 +1,68 @@
+// kernels.h -- internal launch interface between the C ABI layer (attn_api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "attn.h"
+
+namespace attn {
+
+constexpr int kBM = 128;  // query rows per tile (one TMEM lane per row)
+constexpr int kBN = 128;  // keys per tile
+
+// Everything a forward launch needs besides the tensor maps.
+struct FwdParams {
+  void* o;                 // [B,Hq,N,d] or varlen [T,H,d]
+  float* lse;              // [B,Hq,N] or varlen [H,T]; nullable
+  const int32_t* cu_seqlens;  // varlen only
+  unsigned* status;        // device status word
+  int B, Hq, Hkv, N, d, G;
+  int nseq, total_tokens, max_seqlen;
+  int n_qtiles;            // query tiles per (sequence, head): grid extent
+  float scale;             // softmax scale (natural units)
+  float scale_log2;        // scale * log2(e)
+  int out_f32;             // write o as float32
+};
+
+// Tensor maps for the tcgen05 forward: Q, K, V (dense: 3-D {d, N, B*H}; varlen: the same
+// 4-D map {d, H, 3, T} three times).  Boxes are {64, 128(, 1)} with 128-byte swizzle.
+struct FwdMaps {
+  CUtensorMap q, k, v;
+};
+
+cudaError_t launch_fwd_tc(const FwdMaps& maps, const FwdParams& p, attn_dtype_t dtype, bool causal, bool varlen,
+                          cudaStream_t stream);
+cudaError_t launch_fwd_f32(const void* q, const void* k, const void* v, const FwdParams& p, bool causal,
+                           bool varlen, cudaStream_t stream);
+
+// Backward.
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;   // workspace [B,Hq,N,d] fp32
+  float* delta;    // workspace [B,Hq,N] fp32: D_i = dO_i . O_i
+  unsigned* status;
+  int B, Hq, Hkv, N, d, G;
+  int n_ktiles;
+  float scale, scale_log2;
+  int out_f32;
+};
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dout;
+};
+
+cudaError_t launch_bwd_preprocess(const BwdParams& p, attn_dtype_t dtype, bool zero_acc, cudaStream_t stream);
+cudaError_t launch_bwd_postprocess(const BwdParams& p, attn_dtype_t dtype, cudaStream_t stream);
+cudaError_t launch_bwd_tc(const BwdMaps& maps, const BwdParams& p, attn_dtype_t dtype, bool causal,
+                          cudaStream_t stream);
+cudaError_t launch_bwd_f32(const BwdParams& p, bool causal, cudaStream_t stream);
+
+}  // namespace attn

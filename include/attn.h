@@ -1,0 +1,145 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact attention library (libattn_gb300.so).
+ *
+ * The library computes exact scaled-dot-product attention IO-aware: Q.K^T is tiled, the
+ * softmax runs online (running row max and sum) and P.V accumulates on chip, so the N x N
+ * score matrix never reaches HBM.  Sources for what each call computes:
+ *   - "AMD GPU에서도 동작하는 FlashAttention 구현체, Aule-Attention" (jeff.news/article/688),
+ *     API list: tensors [batch, heads, seq_len, head_dim]; causal masks future tokens; scale
+ *     defaults to 1/sqrt(head_dim); head_dim <= 128; float16, bfloat16 and float32; query heads
+ *     a multiple of kv heads (GQA).
+ *   - "跨平台注意力神器AuleAttention把FlashAttention从CUDA解放出来" (jdon.com/83460), sections on
+ *     calling flash_attention (causal forward, loss.backward()) and on GQA / MQA.
+ *   - Turing varlen article (ewbang.com/community/article/details/1000323363), section on the
+ *     core code: flash_attn_varlen_qkvpacked_func's packed qkv [total_tokens,3,heads,head_dim],
+ *     cu_seqlens [batch+1] and output [total_tokens,heads,head_dim].
+ *   - Attention-operator article (m.xxqk.cn/news/636956) section 2.2: Q/K/V tiles staged on
+ *     chip, the softmax max-subtracted in registers, only the output written back.
+ *   - FlashAttention-T review (ai-stack.site), best practices 2 and 4 (scale/mask fused into the
+ *     GEMM loop; online max/sum kept so the backward can restore the normalisation) and FAQ 4
+ *     (the backward recomputes scores rather than storing them).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous, 16-byte
+ *     aligned.  The library allocates no device memory in these calls; the backward's scratch
+ *     is a caller-provided workspace.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream).  Argument errors are returned before anything is launched.
+ *   - Errors found on the device (a pipeline wait that timed out, invalid cu_seqlens) are
+ *     recorded in a per-device status word and returned by attn_get_device_status().
+ *   - scale == 0 selects the default 1/sqrt(d); a negative or NaN scale is rejected.
+ *   - d must be a multiple of 16 in [16, 128]; Hq must be a multiple of Hkv; query head h uses
+ *     kv head h / (Hq / Hkv).
+ *   - dtype selects the element type of q/k/v/o/dout/dq/dk/dv.  ATTN_F16 / ATTN_BF16 run on the
+ *     5th-generation tensor cores (tcgen05) with fp32 accumulation and an fp32 softmax;
+ *     ATTN_F32 runs an fp32 CUDA-core path.
+ *   - flags: ATTN_FLAG_OUT_F32 makes the outputs (o; dq, dk, dv) float32 regardless of dtype:
+ *     the fp32 value the kernel holds before the final rounding to dtype.
+ */
+#ifndef EXACT_ATTENTION_GB300_ATTN_H
+#define EXACT_ATTENTION_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, Hq % Hkv != 0, ... */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid but not provided: d not a multiple of 16 or above 128 */
+  ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (launch, tensor map, ...) */
+  ATTN_ERR_TIMEOUT = 4,      /* device: a pipeline wait exceeded its time limit; CTA stopped */
+  ATTN_ERR_DEVICE_INPUT = 5  /* device: cu_seqlens not non-decreasing from 0, or a sequence
+                                longer than max_seqlen */
+} attn_status_t;
+
+#define ATTN_FLAG_OUT_F32 1u
+
+/*
+ * Forward.
+ *   q    [B, Hq,  N, d]   k, v [B, Hkv, N, d]   (dtype)
+ *   o    [B, Hq,  N, d]   (dtype, or float32 with ATTN_FLAG_OUT_F32)
+ *   lse  [B, Hq,  N] float32, nullable: natural-log log-sum-exp of the scaled, masked scores
+ *        of each query row (LSE_i = m_i + ln sum_j exp(S_ij - m_i)), as the backward needs it.
+ *   causal != 0 masks key j for query i when j > i.
+ * B == 0 or N == 0 is a valid empty call that launches nothing.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                       int Hkv, int N, int d, int causal, float scale, attn_dtype_t dtype, unsigned flags,
+                       void* stream);
+
+/*
+ * Forward on packed variable-length sequences (flash_attn_varlen_qkvpacked_func semantics).
+ *   qkv         [total_tokens, 3, H, d] (dtype): plane 0 = q, 1 = k, 2 = v
+ *   cu_seqlens  DEVICE int32 [nseq + 1]: 0-based prefix sums, cu_seqlens[nseq] == total_tokens;
+ *               sequence s is tokens [cu_seqlens[s], cu_seqlens[s+1]); indices (and the causal
+ *               mask) are relative to the sequence start.  Zero-length sequences are allowed.
+ *   max_seqlen  an upper bound on every sequence length (sizes the launch grid)
+ *   out         [total_tokens, H, d] (dtype, or float32 with ATTN_FLAG_OUT_F32)
+ *   lse         [H, total_tokens] float32, nullable
+ * A cu_seqlens array that is not non-decreasing from 0, or a sequence longer than max_seqlen,
+ * is detected on the device: the affected work is skipped and attn_get_device_status()
+ * returns ATTN_ERR_DEVICE_INPUT.
+ */
+attn_status_t attn_fwd_varlen(const void* qkv, const int32_t* cu_seqlens, int nseq, int total_tokens,
+                              int max_seqlen, void* out, float* lse, int H, int d, int causal, float scale,
+                              attn_dtype_t dtype, unsigned flags, void* stream);
+
+/* Bytes of device workspace attn_bwd needs for these sizes (an fp32 dQ accumulator
+ * [B,Hq,N,d] and the fp32 row terms D_i = dO_i . O_i [B,Hq,N], each 256-byte aligned). */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int d);
+
+/*
+ * Backward: given dout = dL/dO, writes dq [B,Hq,N,d], dk and dv [B,Hkv,N,d] (dtype, or float32
+ * with ATTN_FLAG_OUT_F32).  q, k, v, o are the forward's inputs and output and lse its
+ * float32 LSE; P is recomputed from q, k and lse (nothing of size N x N is stored).  dk and
+ * dv of a kv head sum the contributions of every query head of its group.
+ *   workspace  DEVICE, at least attn_bwd_workspace_bytes(B, Hq, N, d) bytes, 256-byte aligned;
+ *              contents on entry are ignored, on exit undefined.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                       int B, int Hq, int Hkv, int N, int d, int causal, float scale, attn_dtype_t dtype,
+                       unsigned flags, void* stream);
+
+/*
+ * The backward as three steps on one stream (attn_bwd runs all three; calling them separately
+ * lets a caller time or schedule them).  All take the same workspace.
+ *   attn_bwd_prepare: D_i = dO_i . O_i (fp32) into the workspace, and for fp16/bf16 zeroes
+ *                     the fp32 dQ accumulator.
+ *   attn_bwd_main:    the fused recompute-and-reduce kernel: dk, dv (final) and, for
+ *                     fp16/bf16, the dQ accumulator in the workspace.  For ATTN_F32 it writes
+ *                     dq (float32) directly.
+ *   attn_bwd_finish:  dq = scale * accumulator, rounded to dtype (or float32 with
+ *                     ATTN_FLAG_OUT_F32); nothing for ATTN_F32.
+ * The argument rules are those of attn_bwd.
+ */
+attn_status_t attn_bwd_prepare(const void* o, const void* dout, void* workspace, size_t workspace_bytes, int B,
+                               int Hq, int N, int d, attn_dtype_t dtype, void* stream);
+attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, const float* lse, void* dq,
+                            void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                            int N, int d, int causal, float scale, attn_dtype_t dtype, unsigned flags,
+                            void* stream);
+attn_status_t attn_bwd_finish(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int N, int d,
+                              float scale, attn_dtype_t dtype, unsigned flags, void* stream);
+
+/* Synchronises `stream`, then returns and clears the first error the current device's
+ * kernels recorded (ATTN_OK when none).  Returns ATTN_ERR_CUDA if the synchronisation fails. */
+attn_status_t attn_get_device_status(void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/* Library ABI version (major * 100 + minor). */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_GB300_ATTN_H */
