@@ -54,6 +54,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The maximum of a host scalar over all ranks (gloo; host-side timing only)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(flops_per_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica of the step (weak scaling)."""
+    return flops_per_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -337,15 +353,12 @@ def run_ours(args, rank, world, local):
     ms_total = t_start.elapsed_time(t_end)
     per_call_ms = [statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
                    for j in range(launches_per_step)]
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
     st = lib.attn_get_device_status(sp)
     if st != 0:
         raise RuntimeError(f"device status after timed region: {_lib.status_string(st)}")
-    value = step_flops * world / (ms_step * 1e-3) / 1e12
+    value = replica_throughput(step_flops, world, ms_step)
 
     # end to end: pinned host inputs in, results out, inside the timed region
     e2e = None
@@ -373,12 +386,8 @@ def run_ours(args, rank, world, local):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ms_e = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms_e], dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e = float(t.item())
-        e2e = {"value": step_flops * world / (ms_e / Ke * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ms_e = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e = {"value": replica_throughput(step_flops, world, ms_e / Ke), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hin)),
                "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hout)),
                "ms_per_step": ms_e / Ke, "steps": Ke}

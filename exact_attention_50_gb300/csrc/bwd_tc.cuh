@@ -8,16 +8,20 @@
 //
 // One CTA owns one 128-key tile of one (batch, kv head): K and V stay in shared memory, and
 // the CTA walks (query head of the group) x (query tile at or after the key tile when causal).
-// Per query tile, in TMEM (lane = key for the first four, lane = query for dQ):
-//   S^T  = K Q^T      (128 x 128 fp32)       dP^T = V dO^T   (128 x 128 fp32)
-//   dV  += P^T dO     (128 x d, over all iterations)
-//   dK  += dS^T Q     (128 x d, over all iterations)
-//   dQ_t = dS K       (128 x d; reduced into the fp32 workspace with vector atomics)
-// Warps 0-3 turn S^T / dP^T into P^T and dS^T (16-bit, 128-byte swizzled, K-major) in shared
-// memory, then move dQ_t out of TMEM into the workspace; at the end they write dK and dV.
-// Warp 4 is the TMA producer (and TMEM allocator), warp 5 issues the MMAs.
-// The same shared-memory tile serves as a K-major operand in one MMA and as an MN-major
-// operand in another (Q, dO, K, and dS^T read as dS).
+// Per query tile, in TMEM (128 lanes = the 128 keys, except dQ whose lanes are queries):
+//   columns [0,128)     S^T = K Q^T, then P^T (hi and lo 16-bit halves, see below)
+//   columns [128,256)   dP^T = V dO^T, then dQ_t = dS K
+//   columns [256,256+d) dV += P^T dO   (accumulates over every iteration)
+//   columns [256+d, ..) dK += dS^T Q   (accumulates over every iteration)
+// P and dS are split into hi = round16(x) and lo = round16(x - hi) and both halves go through
+// the MMAs, so the gradient contractions see ~16 significant bits of P and dS instead of 8
+// (bf16) or 11 (fp16): rounding P or dS once to bf16 alone already moves causal GQA gradients
+// by ~1e-2.  P^T hi/lo stays in TMEM (A operand of the dV MMA); dS^T hi/lo goes to shared
+// memory, where it is read K-major for dK and, as dS, MN-major for dQ.
+//
+// Warps 0-7: elementwise work, two warps per TMEM lane quadrant, each on half of the 128
+// query columns.  Warp 8: TMA producer and TMEM allocator.  Warp 9: MMA issuer.
+// dQ_t goes from TMEM into the fp32 workspace with 16-byte vector atomics.
 #pragma once
 #include "fwd_tc.cuh"
 
@@ -32,9 +36,9 @@ struct BwdLayout {
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffQ = kOffV + kTileBytes;                 // kQStages tiles
   static constexpr int kOffdO = kOffQ + kQStages * kTileBytes;     // kQStages tiles
-  static constexpr int kOffP = kOffdO + kQStages * kTileBytes;     // P^T  [128 keys x 128 queries]
-  static constexpr int kOffdS = kOffP + 2 * kChunkBytes;           // dS^T [128 keys x 128 queries]
-  static constexpr int kOffRow = kOffdS + 2 * kChunkBytes;         // LSE*log2e and D, 2 buffers each
+  static constexpr int kOffdSh = kOffdO + kQStages * kTileBytes;   // dS^T hi [128 keys x 128 queries]
+  static constexpr int kOffdSl = kOffdSh + 2 * kChunkBytes;        // dS^T lo
+  static constexpr int kOffRow = kOffdSl + 2 * kChunkBytes;        // LSE*log2e and D, 2 buffers each
   static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
   // kv_full, q_full[QS], q_empty[QS], sdp_full, ds_full, dq_full, dq_free, dkdv_done, drain,
   // rows_ready
@@ -43,27 +47,49 @@ struct BwdLayout {
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // TMEM columns
   static constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 256 + DP;
-  static constexpr uint32_t kColdQ = DP == 128 ? 0 : 384;  // d = 128: dQ reuses the S^T columns
+  static constexpr uint32_t kColdQ = kColdP;
+  static constexpr int kThreads = 320;
+  static constexpr int kEwThreads = 256;  // elementwise warps 0-7
 };
 
+// Splits x into hi = round(x) and lo = round(x - hi) in the 16-bit type T, packed in pairs.
+template <typename T>
+__device__ __forceinline__ void split_pack(float a, float b, uint32_t& hi, uint32_t& lo);
+template <>
+__device__ __forceinline__ void split_pack<__nv_bfloat16>(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+template <>
+__device__ __forceinline__ void split_pack<__half>(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 template <typename T, int DP, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const BwdParams p) {
   using L = BwdLayout<DP>;
   constexpr int QS = L::kQStages;
   constexpr int kChunks = DP / 64;
+  constexpr int kEw = L::kEwThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
   uint8_t* sQ = smem + L::kOffQ;
   uint8_t* sdO = smem + L::kOffdO;
-  uint8_t* sP = smem + L::kOffP;
-  uint8_t* sdS = smem + L::kOffdS;
+  uint8_t* sdSh = smem + L::kOffdSh;
+  uint8_t* sdSl = smem + L::kOffdSl;
   float* sLse = reinterpret_cast<float*>(smem + L::kOffRow);  // [2][128]
   float* sD = sLse + 256;                                       // [2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
@@ -96,22 +122,22 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(q_empty + i, 1);
     }
     mbar_init(sdp_full, 1);
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, kEw);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dq_free, kEw);
     mbar_init(dkdv_done, 1);
     mbar_init(drain, 1);
-    mbar_init(rows_ready, 128);
+    mbar_init(rows_ready, kEw);
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 4) tmem_alloc(tmem_slot, L::kTmemCols);
+  if (warp == 8) tmem_alloc(tmem_slot, L::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ================================================================ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -143,7 +169,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ================================================================ MMA issuer
     if (lane == 0) {
       constexpr bool kB = Elem<T>::kBf16;
@@ -151,7 +177,7 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idKD = idesc_f16(kB, false, true, 128, DP);    // dV, dK: B MN-major
       constexpr uint32_t idQ = idesc_f16(kB, true, true, 128, DP);      // dQ: A and B MN-major
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
-      const uint32_t aP = smem_u32(sP), adS = smem_u32(sdS);
+      const uint32_t adSh = smem_u32(sdSh), adSl = smem_u32(sdSl);
       bool ok = mbar_wait(kv_full, 0, abort_flag, p.status);
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % QS;
@@ -174,18 +200,30 @@ __global__ void __launch_bounds__(192, 1)
         mma_commit(sdp_full);
         if (!mbar_wait(ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
+        // dV += P^T dO, P^T hi then lo from TMEM: the 16 queries of k-step ks sit in the 32-column
+        // group ks/2 (hi in its first 16 columns, lo in the last 16), 8 columns per k-step.
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {  // reduction over the 128 queries of the tile
-          const uint32_t a_off = (ks >> 2) * L::kChunkBytes + (ks & 3) * 32;
-          mma_ss(tmem + L::kColdV, smem_desc_sw128(aP + a_off, 16, 1024),
-                 smem_desc_sw128(dobase + ks * 2048, L::kChunkBytes, 1024), idKD, (it > 0 || ks > 0) ? 1u : 0u);
-          mma_ss(tmem + L::kColdK, smem_desc_sw128(adS + a_off, 16, 1024),
-                 smem_desc_sw128(qbase + ks * 2048, L::kChunkBytes, 1024), idKD, (it > 0 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint32_t acol = L::kColS + (ks >> 1) * 32 + (ks & 1) * 8;
+          const uint64_t bd = smem_desc_sw128(dobase + ks * 2048, L::kChunkBytes, 1024);
+          mma_ts(tmem + L::kColdV, tmem + acol, bd, idKD, (it > 0 || ks > 0) ? 1u : 0u);
+          mma_ts(tmem + L::kColdV, tmem + acol + 16, bd, idKD, 1u);
         }
+        // dK += dS^T Q (hi, lo)
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {  // reduction over the 128 keys of the tile
-          mma_ss(tmem + L::kColdQ, smem_desc_sw128(adS + ks * 2048, L::kChunkBytes, 1024),
-                 smem_desc_sw128(aK + ks * 2048, L::kChunkBytes, 1024), idQ, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint32_t a_off = (ks >> 2) * L::kChunkBytes + (ks & 3) * 32;
+          const uint64_t bd = smem_desc_sw128(qbase + ks * 2048, L::kChunkBytes, 1024);
+          mma_ss(tmem + L::kColdK, smem_desc_sw128(adSh + a_off, 16, 1024), bd, idKD, (it > 0 || ks > 0) ? 1u : 0u);
+          mma_ss(tmem + L::kColdK, smem_desc_sw128(adSl + a_off, 16, 1024), bd, idKD, 1u);
+        }
+        // dQ_t = dS K (hi, lo), dS read MN-major from the dS^T tiles
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint64_t bd = smem_desc_sw128(aK + ks * 2048, L::kChunkBytes, 1024);
+          mma_ss(tmem + L::kColdQ, smem_desc_sw128(adSh + ks * 2048, L::kChunkBytes, 1024), bd, idQ,
+                 ks > 0 ? 1u : 0u);
+          mma_ss(tmem + L::kColdQ, smem_desc_sw128(adSl + ks * 2048, L::kChunkBytes, 1024), bd, idQ, 1u);
         }
         mma_commit(dq_full);
         mma_commit(q_empty + st);
@@ -199,10 +237,13 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ================================================================ warps 0-3
-    const int t = threadIdx.x;  // TMEM lane: key row of S^T/dP^T/dK/dV, query row of dQ
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // ================================================================ elementwise warps 0-7
+    const int quad = warp & 3;                // TMEM lane quadrant
+    const int half = warp >> 2;               // query columns [64*half, 64*half+64)
+    const int t = quad * 32 + lane;           // TMEM lane: key row (S^T, dP^T, dK, dV), query row (dQ)
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int key = kt * kBN + t;
+    const bool key_ok = key < N;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
@@ -210,18 +251,17 @@ __global__ void __launch_bounds__(192, 1)
       const size_t row_base = (static_cast<size_t>(b) * p.Hq + h) * N;
       float* lse_buf = sLse + (it & 1) * 128;
       float* d_buf = sD + (it & 1) * 128;
-      {
-        const int q = qt * kBM + t;
-        lse_buf[t] = q < N ? p.lse[row_base + q] * 1.4426950408889634f : INFINITY;
-        d_buf[t] = q < N ? p.delta[row_base + q] : 0.f;
+      if (threadIdx.x < 128) {
+        const int q = qt * kBM + threadIdx.x;
+        lse_buf[threadIdx.x] = q < N ? p.lse[row_base + q] * 1.4426950408889634f : INFINITY;
+        d_buf[threadIdx.x] = q < N ? p.delta[row_base + q] : 0.f;
       }
       mbar_arrive(rows_ready);
       if (!mbar_wait(rows_ready, it & 1, abort_flag, p.status)) { ok = false; break; }
       if (!mbar_wait(sdp_full, it & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      const bool key_ok = key < N;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
         uint32_t rs[32], rd[32];
         tmem_ld32(tl + L::kColS + cc * 32, rs);
         tmem_ld32(tl + L::kColdP + cc * 32, rd);
@@ -238,28 +278,31 @@ __global__ void __launch_bounds__(192, 1)
           pv[i] = pr;
           dsv[i] = pr * (__uint_as_float(rd[i]) - d_buf[qi]);
         }
-        // 32 queries = 4 16-byte granules of this key's 256-byte P^T / dS^T row
+        // P^T hi/lo back into the 32 S^T columns just read: hi in the first 16, lo in the last 16
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) split_pack<T>(pv[2 * i], pv[2 * i + 1], ph[i], pl[i]);
+        tmem_st16(tl + L::kColS + cc * 32, ph);
+        tmem_st16(tl + L::kColS + cc * 32 + 16, pl);
+        // dS^T hi/lo -> shared memory, K-major with the 128-byte swizzle
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) {
-          const int gq = cc * 4 + gi;  // granule index over 128 queries
+          const int gq = cc * 4 + gi;  // 16-byte granule index over the 128 queries
           const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
           uint4 a, c;
-          a.x = Elem<T>::pack(pv[gi * 8 + 0], pv[gi * 8 + 1]);
-          a.y = Elem<T>::pack(pv[gi * 8 + 2], pv[gi * 8 + 3]);
-          a.z = Elem<T>::pack(pv[gi * 8 + 4], pv[gi * 8 + 5]);
-          a.w = Elem<T>::pack(pv[gi * 8 + 6], pv[gi * 8 + 7]);
-          c.x = Elem<T>::pack(dsv[gi * 8 + 0], dsv[gi * 8 + 1]);
-          c.y = Elem<T>::pack(dsv[gi * 8 + 2], dsv[gi * 8 + 3]);
-          c.z = Elem<T>::pack(dsv[gi * 8 + 4], dsv[gi * 8 + 5]);
-          c.w = Elem<T>::pack(dsv[gi * 8 + 6], dsv[gi * 8 + 7]);
-          *reinterpret_cast<uint4*>(sP + off) = a;
-          *reinterpret_cast<uint4*>(sdS + off) = c;
+          split_pack<T>(dsv[gi * 8 + 0], dsv[gi * 8 + 1], a.x, c.x);
+          split_pack<T>(dsv[gi * 8 + 2], dsv[gi * 8 + 3], a.y, c.y);
+          split_pack<T>(dsv[gi * 8 + 4], dsv[gi * 8 + 5], a.z, c.z);
+          split_pack<T>(dsv[gi * 8 + 6], dsv[gi * 8 + 7], a.w, c.w);
+          *reinterpret_cast<uint4*>(sdSh + off) = a;
+          *reinterpret_cast<uint4*>(sdSl + off) = c;
         }
       }
+      tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(ds_full);
-      // dQ_t (lane = query row) -> fp32 workspace
+      // dQ_t (lane = query row) -> fp32 workspace; this warp takes half of the d columns
       if (!mbar_wait(dq_full, it & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       {
@@ -267,7 +310,7 @@ __global__ void __launch_bounds__(192, 1)
         float* dst = p.dq_acc + (row_base + q) * static_cast<size_t>(p.d);
         uint32_t r[32];
 #pragma unroll
-        for (int c = 0; c < DP / 32; ++c) {
+        for (int c = half * (DP / 64); c < (half + 1) * (DP / 64); ++c) {
           tmem_ld32(tl + L::kColdQ + c * 32, r);
           tmem_ld_wait();
           tmem_reg_fence(r);
@@ -276,16 +319,15 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               if (i * 4 < ncol)
-                atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + i * 4),
-                          make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                      __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+                red_add_v4(dst + c * 32 + i * 4, __uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
           }
         }
       }
       tc_fence_before();
       mbar_arrive(dq_free);
     }
-    // ---- epilogue: dK (scaled) and dV rows of this key tile
+    // ---- epilogue: dK (scaled) and dV rows of this key tile, half of the columns per warp
     if (ok && mbar_wait(dkdv_done, 0, abort_flag, p.status)) {
       tc_fence_after();
       const size_t krow = (static_cast<size_t>(b) * p.Hkv + g) * N + key;
@@ -296,11 +338,11 @@ __global__ void __launch_bounds__(192, 1)
         void* out = which == 0 ? p.dk : p.dv;
         uint32_t r[32];
 #pragma unroll
-        for (int c = 0; c < DP / 32; ++c) {
+        for (int c = half * (DP / 64); c < (half + 1) * (DP / 64); ++c) {
           tmem_ld32(tl + col + c * 32, r);
           tmem_ld_wait();
           tmem_reg_fence(r);
-          if (key < N && c * 32 < p.d) {
+          if (key_ok && c * 32 < p.d) {
             const int ncol = min(32, p.d - c * 32);
             if (p.out_f32) {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + krow * p.d + c * 32);
@@ -330,7 +372,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -343,7 +385,7 @@ cudaError_t launch_bwd_tc_t(const BwdMaps& maps, const BwdParams& p, cudaStream_
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.n_ktiles, p.B * p.Hkv);
-  kern<<<grid, 192, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, maps.dout, p);
+  kern<<<grid, L::kThreads, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, maps.dout, p);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,5 @@
-// fwd_tc.cuh -- tcgen05 forward for fp16 / bf16: TMA-fed, warp-specialised, S and O in TMEM.
+// fwd_tc.cuh -- tcgen05 forward for fp16 / bf16: persistent, TMA-fed, warp-specialised, two
+// 128-row query tiles per CTA sharing every K/V tile, S / P / O in TMEM.
 //
 // What it computes (per query row i of a (batch, head) or (sequence, head)):
 //   S_ij = scale * Q_i . K_j, masked to -inf for j > i (causal) and for keys past the sequence;
@@ -9,19 +10,26 @@
 // The online max/sum update follows the FlashAttention-T review, best practice 4; scale and
 // mask are applied inside the GEMM loop as in its best practice 2.
 //
-// One CTA = one 128-row query tile, 6 warps:
-//   warps 0-3  softmax: thread t owns query row t (TMEM lane t); loads its S row from TMEM,
-//              masks, updates m/l, writes P (16-bit, 128-byte swizzled) to shared memory,
-//              rescales its O row in TMEM when the max moved, and runs the epilogue.
-//   warp 4     TMA producer (lane 0) and TMEM allocator (whole warp).
-//   warp 5     MMA issuer (lane 0): S_j = Q K_j^T into one of two TMEM S buffers, then
-//              O += P_{j-1} V_{j-1}; each group is committed to an mbarrier.
-// TMEM: S buffers at columns [0,128) and [128,256), O at [256, 256+DP).
-// K and V stream through separate STAGES-deep rings; Q is loaded once.
+// A CTA loops over work items (a pair of consecutive 128-row query tiles A and B of one
+// (batch, head) or (sequence, head)), heaviest first under the causal mask.  320 threads:
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t of a group owns query
+//              row t (TMEM lane t); loads its S row, masks, updates m / l, writes P (16-bit) back
+//              over the first 64 columns of its own S row, rescales its O row when the max moved,
+//              and writes O / l and the LSE at the end of the item.
+//   warp 8     TMA producer (lane 0) and TMEM allocator (whole warp).
+//   warp 9     MMA issuer (lane 0).  Per key tile j, in order:
+//                PV_A(j-1) ; S_A(j) ; PV_B(j-1) ; S_B(j)
+//              so that while one group computes its softmax the tensor core works on the
+//              other tile.  S_X(j) overwrites P_X(j-1), so it is issued only after PV_X(j-1)
+//              has completed (its mbarrier), never just after it in program order.
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+DP), O_B [256+DP, 256+2DP).
+// Shared memory: Q_A, Q_B, and STAGES-deep K and V rings.
 //
 // Lazy rescaling: the running max used for the exponentials is only moved when a tile's max
-// exceeds it by more than kRescaleLog2 (in log2 units); the final O / l and LSE use the same
-// max, so the result is exact, and P stays below 2^kRescaleLog2 (well inside fp16 range).
+// exceeds it by more than kRescaleLog2 (log2 units); the final O / l and LSE use the same max,
+// so the result is exact, and P stays below 2^kRescaleLog2 (well inside fp16 range).  Because
+// S_X(j) is issued after PV_X(j-1) completed, a softmax group that sees S_X(j) may rescale O_X
+// at once.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -53,21 +61,26 @@ constexpr float kRescaleLog2 = 8.0f;
 
 template <int DP>
 struct FwdLayout {
-  static constexpr int kStages = DP == 128 ? 2 : 3;
+  static constexpr int kStages = DP == 128 ? 2 : 4;
   static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 64 elements x 2 B
   static constexpr int kTileBytes = (DP / 64) * kChunkBytes;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffQ = 0;                        // Q_A then Q_B
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kChunkBytes;
-  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], s_free[2],
-  //           p_full, o_done, drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 3;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
+  // pv_done[2], o_free[2], drain
+  static constexpr int kNumBars = 2 + 4 * kStages + 8 + 1;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base (u32), abort flag (int)
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;         // slack for 1024-byte alignment
   static constexpr uint32_t kTmemCols = 512;
+  // 3 warpgroups: softmax A, softmax B, and producer / MMA (+2 idle warps).  Launched at
+  // kLaunchRegs registers per thread; the producer warpgroup gives registers to the softmax
+  // warpgroups (kRegsLow + 2 * kRegsHigh == 3 * kLaunchRegs).
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kLaunchRegs = 168, kRegsLow = 72, kRegsHigh = 216;
+  static_assert(kRegsLow + 2 * kRegsHigh == 3 * kLaunchRegs, "register split must match the launch");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -76,10 +89,50 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>(a + ((1024u - (s & 1023u)) & 1023u));
 }
 
+// One work item: a pair of 128-row query tiles (rows [256*pair, 256*pair+256) of a sequence).
+struct FwdItem {
+  int b, h, pair, seq_start, seq_len, n_kv;
+  bool valid;
+};
+
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int idx) {
+  FwdItem it;
+  const int heads = VARLEN ? p.Hq : p.B * p.Hq;
+  const int per_pair = VARLEN ? heads * p.nseq : heads;
+  it.pair = p.n_qtiles - 1 - idx / per_pair;  // n_qtiles counts pairs here; heaviest first
+  const int rem = idx % per_pair;
+  it.valid = true;
+  if constexpr (VARLEN) {
+    const int s = rem / heads;
+    it.h = rem % heads;
+    it.b = 0;
+    const int c0 = p.cu_seqlens[s], c1 = p.cu_seqlens[s + 1];
+    const bool bad = c0 < 0 || c1 < c0 || c1 > p.total_tokens || c1 - c0 > p.max_seqlen ||
+                     (s == 0 && c0 != 0) || (s == p.nseq - 1 && c1 != p.total_tokens);
+    if (bad) {
+      if (it.pair == 0 && it.h == 0) raise_status(p.status, ATTN_ERR_DEVICE_INPUT);
+      it.valid = false;
+    }
+    it.seq_start = c0;
+    it.seq_len = c1 - c0;
+    if (it.pair * 2 * kBM >= it.seq_len) it.valid = false;
+  } else {
+    it.b = rem / p.Hq;
+    it.h = rem % p.Hq;
+    it.seq_start = 0;
+    it.seq_len = p.N;
+  }
+  const int n_kv_all = (it.seq_len + kBN - 1) / kBN;
+  it.n_kv = CAUSAL ? min(2 * it.pair + 2, n_kv_all) : n_kv_all;
+  if (it.n_kv <= 0) it.valid = false;
+  return it;
+}
+
 template <typename T, int DP, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p, int n_items) {
   using L = FwdLayout<DP>;
   constexpr int S = L::kStages;
   constexpr int kChunks = DP / 64;
@@ -88,52 +141,26 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sQ = smem + L::kOffQ;
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
-  uint8_t* sP = smem + L::kOffP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
   uint64_t* k_empty = k_full + S;
   uint64_t* v_full = k_empty + S;
   uint64_t* v_empty = v_full + S;
-  uint64_t* s_full = v_empty + S;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* drain = o_done + 1;
+  uint64_t* s_full = v_empty + S;   // [2]: tile A, tile B
+  uint64_t* p_full = s_full + 2;    // [2]
+  uint64_t* pv_done = p_full + 2;   // [2]
+  uint64_t* o_free = pv_done + 2;   // [2]
+  uint64_t* drain = o_free + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- which tile this CTA computes
-  int b = 0, h, qt, seq_start = 0, seq_len;
-  if constexpr (VARLEN) {
-    h = blockIdx.x;
-    const int s = blockIdx.z;
-    qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);
-    const int c0 = p.cu_seqlens[s], c1 = p.cu_seqlens[s + 1];
-    const bool bad = c0 < 0 || c1 < c0 || c1 > p.total_tokens || c1 - c0 > p.max_seqlen ||
-                     (s == 0 && c0 != 0) || (s == p.nseq - 1 && c1 != p.total_tokens);
-    if (bad) {
-      if (threadIdx.x == 0) raise_status(p.status, ATTN_ERR_DEVICE_INPUT);
-      return;
-    }
-    seq_start = c0;
-    seq_len = c1 - c0;
-    if (qt * kBM >= seq_len) return;
-  } else {
-    b = blockIdx.x / p.Hq;
-    h = blockIdx.x % p.Hq;
-    qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);
-    seq_len = p.N;
-  }
-  const int g = h / p.G;
-  const int n_kv_all = (seq_len + kBN - 1) / kBN;
-  const int n_kv = CAUSAL ? min(qt + 1, n_kv_all) : n_kv_all;
-
-  // ---- setup
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int i = 0; i < S; ++i) {
       mbar_init(k_full + i, 1);
       mbar_init(k_empty + i, 1);
@@ -142,222 +169,267 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(s_free + i, 128);
+      mbar_init(p_full + i, 128);
+      mbar_init(pv_done + i, 1);
+      mbar_init(o_free + i, 128);
     }
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 4) tmem_alloc(tmem_slot, L::kTmemCols);
+  if (warp == 8) tmem_alloc(tmem_slot, L::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp == 4) {
+  // Each register-budget change opens its own branch, which runs to the teardown.
+  if (warp >= 8) {
+  regs_dec<L::kRegsLow>();
+  if (warp >= 10) {
+    // spare warps of the producer warpgroup: nothing to do
+  } else if (warp == 8) {
     // ================================================================ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const uint32_t tile_bytes = L::kTileBytes;
-      mbar_expect_tx(q_full, tile_bytes);
-      for (int c = 0; c < kChunks; ++c) {
-        if constexpr (VARLEN)
-          tma_load_4d(sQ + c * L::kChunkBytes, &tmQ, q_full, c * 64, h, 0, seq_start + qt * kBM);
-        else
-          tma_load_3d(sQ + c * L::kChunkBytes, &tmQ, q_full, c * 64, qt * kBM, b * p.Hq + h);
-      }
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % S;
-        const uint32_t ph = ((j / S) - 1) & 1;
-        if (j >= S && !mbar_wait(k_empty + st, ph, abort_flag, p.status)) break;
-        mbar_expect_tx(k_full + st, tile_bytes);
-        for (int c = 0; c < kChunks; ++c) {
-          uint8_t* dst = sK + st * L::kTileBytes + c * L::kChunkBytes;
-          if constexpr (VARLEN)
-            tma_load_4d(dst, &tmK, k_full + st, c * 64, h, 1, seq_start + j * kBN);
-          else
-            tma_load_3d(dst, &tmK, k_full + st, c * 64, j * kBN, b * p.Hkv + g);
+      uint32_t kv = 0;  // key tiles issued so far (ring position), across items
+      uint32_t ic = 0;  // items processed
+      uint32_t nk_issued = 0, nv_issued = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
+        if (!it.valid) continue;
+        if (ic > 0 && !mbar_wait(q_empty, (ic - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        mbar_expect_tx(q_full, 2 * L::kTileBytes);
+        for (int x = 0; x < 2; ++x) {
+          const int row0 = (2 * it.pair + x) * kBM;
+          for (int c = 0; c < kChunks; ++c) {
+            uint8_t* dst = sQ + x * L::kTileBytes + c * L::kChunkBytes;
+            if constexpr (VARLEN)
+              tma_load_4d(dst, &tmQ, q_full, c * 64, it.h, 0, it.seq_start + row0);
+            else
+              tma_load_3d(dst, &tmQ, q_full, c * 64, row0, it.b * p.Hq + it.h);
+          }
         }
-        if (j >= S && !mbar_wait(v_empty + st, ph, abort_flag, p.status)) {
-          issued = 2 * j + 1;
-          break;
+        const int g = it.h / p.G;
+        for (int j = 0; j < it.n_kv; ++j, ++kv) {
+          const int st = kv % S;
+          const uint32_t ph = ((kv / S) - 1) & 1;
+          if (kv >= S && !mbar_wait(k_empty + st, ph, abort_flag, p.status)) { ok = false; break; }
+          mbar_expect_tx(k_full + st, L::kTileBytes);
+          for (int c = 0; c < kChunks; ++c) {
+            uint8_t* dst = sK + st * L::kTileBytes + c * L::kChunkBytes;
+            if constexpr (VARLEN)
+              tma_load_4d(dst, &tmK, k_full + st, c * 64, it.h, 1, it.seq_start + j * kBN);
+            else
+              tma_load_3d(dst, &tmK, k_full + st, c * 64, j * kBN, it.b * p.Hkv + g);
+          }
+          nk_issued = kv + 1;
+          if (kv >= S && !mbar_wait(v_empty + st, ph, abort_flag, p.status)) { ok = false; break; }
+          mbar_expect_tx(v_full + st, L::kTileBytes);
+          for (int c = 0; c < kChunks; ++c) {
+            uint8_t* dst = sV + st * L::kTileBytes + c * L::kChunkBytes;
+            if constexpr (VARLEN)
+              tma_load_4d(dst, &tmV, v_full + st, c * 64, it.h, 2, it.seq_start + j * kBN);
+            else
+              tma_load_3d(dst, &tmV, v_full + st, c * 64, j * kBN, it.b * p.Hkv + g);
+          }
+          nv_issued = kv + 1;
         }
-        mbar_expect_tx(v_full + st, tile_bytes);
-        for (int c = 0; c < kChunks; ++c) {
-          uint8_t* dst = sV + st * L::kTileBytes + c * L::kChunkBytes;
-          if constexpr (VARLEN)
-            tma_load_4d(dst, &tmV, v_full + st, c * 64, h, 2, seq_start + j * kBN);
-          else
-            tma_load_3d(dst, &tmV, v_full + st, c * 64, j * kBN, b * p.Hkv + g);
-        }
-        issued = 2 * j + 2;
+        ++ic;
       }
       if (*abort_flag) {
         // let the copies already issued land before the CTA's shared memory goes away
-        mbar_drain(q_full, 0);
-        const int nk = (issued + 1) / 2, nv = issued / 2;
-        for (int j = max(0, nk - S); j < nk; ++j) mbar_drain(k_full + j % S, (j / S) & 1);
-        for (int j = max(0, nv - S); j < nv; ++j) mbar_drain(v_full + j % S, (j / S) & 1);
+        if (ic > 0) mbar_drain(q_full, (ic - 1) & 1);
+        for (uint32_t j = nk_issued > (uint32_t)S ? nk_issued - S : 0; j < nk_issued; ++j)
+          mbar_drain(k_full + j % S, (j / S) & 1);
+        for (uint32_t j = nv_issued > (uint32_t)S ? nv_issued - S : 0; j < nv_issued; ++j)
+          mbar_drain(v_full + j % S, (j / S) & 1);
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ================================================================ MMA issuer
     if (lane == 0) {
       constexpr bool kB = Elem<T>::kBf16;
       constexpr uint32_t idS = idesc_f16(kB, false, false, 128, kBN);
       constexpr uint32_t idO = idesc_f16(kB, false, true, 128, DP);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
-      const uint32_t tO = tmem + 256;
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-      auto issue_pv = [&](int jj) -> bool {
-        if (!mbar_wait(p_full, jj & 1, abort_flag, p.status)) return false;
-        const int st = jj % S;
-        if (!mbar_wait(v_full + st, (jj / S) & 1, abort_flag, p.status)) return false;
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
+      uint32_t ic = 0;
+      bool ok = true;
+      // Descriptors are built once; a k-step adds its byte offset >> 4 to the start-address
+      // field (shared addresses stay below 256 KB, so the 14-bit field never carries).
+      const uint64_t dQ = smem_desc_sw128(aQ, 16, 1024);
+      const uint64_t dK = smem_desc_sw128(aK, 16, 1024);
+      const uint64_t dV = smem_desc_sw128(aV, L::kChunkBytes, 1024);
+      auto issue_s = [&](int x, uint32_t t) -> bool {
+        // S_x for global tile t: P_x of tile t-1 must have been consumed by PV_x(t-1)
+        if (t > 0 && !mbar_wait(pv_done + x, (t - 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t a = smem_desc_sw128(aP + (ks >> 2) * L::kChunkBytes + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(aV + st * L::kTileBytes + ks * 2048, L::kChunkBytes, 1024);
-          mma_ss(tO, a, bd, idO, (jj > 0 || ks > 0) ? 1u : 0u);
+        const uint64_t qx = dQ + ((x * L::kTileBytes) >> 4);
+        const uint64_t kx = dK + (((t % S) * L::kTileBytes) >> 4);
+#pragma unroll 1
+        for (int ks = 0; ks < DP / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + x * 128, qx + off, kx + off, idS, ks > 0 ? 1u : 0u);
         }
-        mma_commit(o_done);
-        mma_commit(v_empty + st);
+        mma_commit(s_full + x);
         return true;
       };
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % S;
-        const int sb = j & 1;
-        if (!mbar_wait(k_full + st, (j / S) & 1, abort_flag, p.status)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(s_free + sb, ((j >> 1) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      auto issue_pv = [&](int x, uint32_t t, bool first, bool last_of_pair) -> bool {
+        if (!mbar_wait(p_full + x, t & 1, abort_flag, p.status)) return false;
+        if (first && ic > 0 && !mbar_wait(o_free + x, (ic - 1) & 1, abort_flag, p.status)) return false;
+        const int st = t % S;
+        if (!mbar_wait(v_full + st, (t / S) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < DP / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * L::kChunkBytes + (ks & 3) * 32;
-          const uint64_t a = smem_desc_sw128(aQ + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(aK + st * L::kTileBytes + off, 16, 1024);
-          mma_ss(tmem + sb * 128, a, bd, idS, ks > 0 ? 1u : 0u);
+        const uint32_t tO = tmem + 256 + x * DP;
+        const uint64_t vx = dV + ((st * L::kTileBytes) >> 4);
+#pragma unroll 1
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          mma_ts(tO, tmem + x * 128 + ks * 8, vx + ((ks * 2048) >> 4), idO, (!first || ks > 0) ? 1u : 0u);
         }
-        mma_commit(s_full + sb);
-        mma_commit(k_empty + st);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        mma_commit(pv_done + x);
+        if (last_of_pair) mma_commit(v_empty + st);
+        return true;
+      };
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
+        if (!it.valid) continue;
+        if (!mbar_wait(q_full, ic & 1, abort_flag, p.status)) { ok = false; break; }
+        const uint32_t t0 = kv;
+        // prologue: S_A(0), S_B(0)
+        if (!mbar_wait(k_full + t0 % S, (t0 / S) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!issue_s(0, t0) || !issue_s(1, t0)) { ok = false; break; }
+        mma_commit(k_empty + t0 % S);
+        if (it.n_kv == 1) mma_commit(q_empty);  // the item's last MMA reading Q_A / Q_B is issued
+        for (int j = 0; j < it.n_kv; ++j) {
+          const uint32_t t = t0 + j;
+          const bool more = j + 1 < it.n_kv;
+          if (!issue_pv(0, t, j == 0, false)) { ok = false; break; }
+          if (more) {
+            if (!mbar_wait(k_full + (t + 1) % S, ((t + 1) / S) & 1, abort_flag, p.status)) { ok = false; break; }
+            if (!issue_s(0, t + 1)) { ok = false; break; }
+          }
+          if (!issue_pv(1, t, j == 0, true)) { ok = false; break; }
+          if (more) {
+            if (!issue_s(1, t + 1)) { ok = false; break; }
+            mma_commit(k_empty + (t + 1) % S);
+            if (j + 2 == it.n_kv) mma_commit(q_empty);  // last MMA reading Q_A / Q_B issued
+          }
+        }
+        if (!ok) break;
+        kv = t0 + it.n_kv;
+        ++ic;
       }
-      if (ok) ok = issue_pv(n_kv - 1);
       if (!ok) {
         mma_commit(drain);  // every MMA issued so far completes before this arrives
         mbar_drain(drain, 0);
       }
     }
     __syncwarp();
+  }
   } else {
-    // ================================================================ softmax warps 0-3
-    const int row = threadIdx.x;  // 0..127 == TMEM lane
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int q_row = qt * kBM + row;  // relative to the sequence
+    regs_inc<L::kRegsHigh>();
+    // ================================================================ softmax groups
+    const int x = warp >> 2;                  // 0 = tile A, 1 = tile B
+    const int row = threadIdx.x & 127;        // TMEM lane
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t tS = tl + x * 128, tO = tl + 256 + x * DP;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    uint32_t kv = 0, ic = 0;
     bool ok = true;
-    uint8_t* prow = sP + row * 128;
-    for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(s_full + sb, (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-      tc_fence_after();
-      float s[kBN];
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          tmem_ld32(tl + sb * 128 + c * 32, r);
-          tmem_ld_wait();
-          tmem_reg_fence(r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(s_free + sb);
-
-      const int key0 = j * kBN;
-      if ((CAUSAL && key0 + kBN - 1 > q_row) || key0 + kBN > seq_len) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const int key = key0 + c;
-          if ((CAUSAL && key > q_row) || key >= seq_len) s[c] = -INFINITY;
-        }
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-      const float mx2 = mx * sl2;  // scale > 0: max commutes with the scaling
-      float alpha = 1.f;
-      bool resc = false;
-      if (mx2 > m + kRescaleLog2 || (m == -INFINITY && mx2 != -INFINITY)) {
-        alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mx2);
-        resc = (j > 0) && (m != -INFINITY);
-        m = mx2;
-      }
-      const float mb = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        s[c] = ex2_approx(fmaf(s[c], sl2, -mb));
-        rs += s[c];
-      }
-      l = l * alpha + rs;
-
-      if (j >= 1) {
-        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+      const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
+      if (!it.valid) continue;
+      const int q_row = (2 * it.pair + x) * kBM + row;  // relative to the sequence
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < it.n_kv; ++j) {
+        const uint32_t t = kv + j;
+        if (!mbar_wait(s_full + x, t & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
+        float s[kBN];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < kBN / 32; ++c) {
+            tmem_ld32(tS + c * 32, r);
+            tmem_ld_wait();
+            tmem_reg_fence(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+          }
+        }
+        // keys key0 + c with c > lim are masked (past the diagonal, or past the sequence)
+        const int key0 = j * kBN;
+        const int lim = CAUSAL ? min(q_row, it.seq_len - 1) - key0 : it.seq_len - 1 - key0;
+        if (lim < kBN - 1) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) s[c] = c > lim ? -INFINITY : s[c];
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+        const float mx2 = mx * sl2;  // scale > 0: max commutes with the scaling
+        float alpha = 1.f;
+        bool resc = false;
+        if (mx2 > m + kRescaleLog2 || (m == -INFINITY && mx2 != -INFINITY)) {
+          alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mx2);
+          resc = (j > 0) && (m != -INFINITY);
+          m = mx2;
+        }
+        const float mb = (m == -INFINITY) ? 0.f : m;
+        float rs = 0.f;
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          const float e0 = ex2_approx(fmaf(s[c], sl2, -mb));
+          const float e1 = ex2_approx(fmaf(s[c + 1], sl2, -mb));
+          rs += e0 + e1;
+          pk[c / 2] = Elem<T>::pack(e0, e1);
+        }
+        l = l * alpha + rs;
+        // P row over the first 64 columns of this row's S (keys 2c, 2c+1 in column c)
+#pragma unroll
+        for (int c = 0; c < kBN / 64; ++c) {
+          tmem_st32(tS + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + c * 32));
+        }
+        // O_x *= alpha (after the S row is dead, to keep registers low): PV_x(t-1) has completed
+        // (S_x(t) was issued after it) and PV_x(t) waits for p_full below
         if (__any_sync(0xffffffffu, resc)) {
           const float a = resc ? alpha : 1.f;
           uint32_t r[32];
 #pragma unroll
           for (int c = 0; c < DP / 32; ++c) {
-            tmem_ld32(tl + 256 + c * 32, r);
+            tmem_ld32(tO + c * 32, r);
             tmem_ld_wait();
             tmem_reg_fence(r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
-            tmem_st32(tl + 256 + c * 32, r);
+            tmem_st32(tO + c * 32, r);
           }
-          tmem_st_wait();
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + x);
       }
-      // P row -> shared memory, K-major with the 128-byte swizzle (16-byte granule g of a
-      // 128-byte row r lands at granule g ^ (r & 7)).
-#pragma unroll
-      for (int gi = 0; gi < kBN / 8; ++gi) {
-        uint4 v;
-        v.x = Elem<T>::pack(s[gi * 8 + 0], s[gi * 8 + 1]);
-        v.y = Elem<T>::pack(s[gi * 8 + 2], s[gi * 8 + 3]);
-        v.z = Elem<T>::pack(s[gi * 8 + 4], s[gi * 8 + 5]);
-        v.w = Elem<T>::pack(s[gi * 8 + 6], s[gi * 8 + 7]);
-        uint8_t* dst = prow + (gi >> 3) * L::kChunkBytes + ((((gi & 7) ^ (row & 7))) << 4);
-        *reinterpret_cast<uint4*>(dst) = v;
-      }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    // ---- epilogue: O / l and LSE
-    if (ok && n_kv > 0 && mbar_wait(o_done, (n_kv - 1) & 1, abort_flag, p.status)) {
+      if (!ok) break;
+      kv += it.n_kv;
+      // ---- epilogue: O / l and LSE, then release O_x for the next item's first PV
+      if (!mbar_wait(pv_done + x, (kv - 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      const bool valid = q_row < seq_len;
+      const bool valid = q_row < it.seq_len;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       size_t row_off;
       if constexpr (VARLEN)
-        row_off = (static_cast<size_t>(seq_start + q_row) * p.Hq + h) * p.d;
+        row_off = (static_cast<size_t>(it.seq_start + q_row) * p.Hq + it.h) * p.d;
       else
-        row_off = ((static_cast<size_t>(b) * p.Hq + h) * p.N + q_row) * p.d;
+        row_off = ((static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row) * p.d;
       uint32_t r[32];
 #pragma unroll
       for (int c = 0; c < DP / 32; ++c) {
-        tmem_ld32(tl + 256 + c * 32, r);
+        tmem_ld32(tO + c * 32, r);
         tmem_ld_wait();
         tmem_reg_fence(r);
         const int col0 = c * 32;
@@ -387,37 +459,57 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(o_free + x);
       if (valid && p.lse) {
         const float lse = (m + __log2f(l)) * 0.69314718055994531f;
         if constexpr (VARLEN)
-          p.lse[static_cast<size_t>(h) * p.total_tokens + seq_start + q_row] = lse;
+          p.lse[static_cast<size_t>(it.h) * p.total_tokens + it.seq_start + q_row] = lse;
         else
-          p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.N + q_row] = lse;
+          p.lse[(static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row] = lse;
       }
+      ++ic;
     }
   }
 
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
 }
 
+inline int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 148;
+  }
+  return n;
+}
+
 template <typename T, int DP, bool CAUSAL, bool VARLEN>
-cudaError_t launch_fwd_tc_t(const FwdMaps& maps, const FwdParams& p, cudaStream_t stream) {
+cudaError_t launch_fwd_tc_t(const FwdMaps& maps, const FwdParams& p_in, cudaStream_t stream) {
   using L = FwdLayout<DP>;
   auto kern = fwd_tc_kernel<T, DP, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  dim3 grid;
-  if (VARLEN)
-    grid = dim3(p.Hq, p.n_qtiles, p.nseq);
-  else
-    grid = dim3(p.B * p.Hq, p.n_qtiles, 1);
-  kern<<<grid, 192, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, p);
+  // The in-kernel register split assumes the launch allocation; never launch otherwise (an
+  // increase beyond what the block holds would wait forever).
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != static_cast<int>(L::kLaunchRegs)) return cudaErrorInvalidConfiguration;
+  FwdParams p = p_in;
+  p.n_qtiles = (p_in.n_qtiles + 1) / 2;  // pairs of query tiles
+  const long heads = VARLEN ? static_cast<long>(p.Hq) * p.nseq : static_cast<long>(p.B) * p.Hq;
+  const long items = heads * p.n_qtiles;
+  if (items > 0x7fffffffL) return cudaErrorInvalidValue;
+  const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
+  kern<<<grid, L::kThreads, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, p, static_cast<int>(items));
   return cudaGetLastError();
 }
 

@@ -71,10 +71,11 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(const float* __restrict__ 
   const int d = p.d, g = h / p.G;
   RowAddr qa, ka, va;
   if constexpr (VARLEN) {
+    // q, k and v already point at planes 0, 1 and 2 of the packed [T,3,H,d] tensor
     const size_t tok = 3ull * p.Hq * d;
     qa = {static_cast<size_t>(seq_start) * tok + static_cast<size_t>(h) * d, tok};
-    ka = {qa.base + static_cast<size_t>(p.Hq) * d, tok};
-    va = {qa.base + 2ull * p.Hq * d, tok};
+    ka = qa;
+    va = qa;
   } else {
     qa = {(static_cast<size_t>(b) * p.Hq + h) * p.N * d, static_cast<size_t>(d)};
     ka = {(static_cast<size_t>(b) * p.Hkv + g) * p.N * d, static_cast<size_t>(d)};

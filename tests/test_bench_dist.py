@@ -1,0 +1,51 @@
+"""The benchmark's multi-rank host logic on CPU with gloo, world size 2: replicas report the
+maximum time over ranks, throughput aggregates over ranks, and the reference arm runs on rank 0
+only while the other rank exits without work."""
+import multiprocessing as mp
+import os
+import socket
+
+import pytest
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        t = bench.max_over_ranks(1.5 + rank, world)
+        args = bench.parse_args(["--impl", "reference", "--workload", "tiny_f32", "--steps", "1", "--warmup", "1"])
+        line = bench.run_reference(args, rank, world)
+        q.put((rank, t, None if line is None else (line["impl"], line["n_gpus"], line["value"] > 0)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_max_time_and_reference_on_rank0_only():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = dict((r, (t, line)) for r, t, line in (q.get(timeout=240) for _ in procs))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out[0][0] == out[1][0] == 2.5
+    assert out[0][1] == ("reference", 2, True)
+    assert out[1][1] is None
+
+
+def test_replica_throughput_is_whole_job():
+    import bench
+    assert bench.replica_throughput(1e12, 4, 1000.0) == pytest.approx(4.0)
+    assert bench.max_over_ranks(3.0, 1) == 3.0

@@ -104,7 +104,24 @@ def test_online_rescaling_under_growing_scores(dev, d, causal):
     dout = torch.randn(B, H, N, d, generator=g)
     q, k, v, dout = (t.to(torch.bfloat16) for t in (q, k, v, dout))
     res = gpu_fwd_bwd(q, k, v, dout, causal, None, dev)
-    check_dense(res, q, k, v, dout, causal, None, torch.bfloat16, f"rescale d={d} causal={causal}")
+    what = f"rescale d={d} causal={causal}"
+    check_dense(res, q, k, v, dout, causal, None, torch.bfloat16, what, with_bwd=False)
+    # Backward.  D_i = dO_i . O_i uses the stored bf16 O, off by at most 2^-9 sum_c |dO_ic O_ic|
+    # (round to nearest); through dS_ij = P_ij (dP_ij - D_i) that moves dQ_i by
+    # scale * dD_i * sum_j P_ij K_j, which these large-offset keys make larger than with N(0,1)
+    # inputs.  dV does not involve D; dK gets it only through sign-mixed sums over i.
+    qn, kn, vn, dn = (to_np(t) for t in (q, k, v, dout))
+    sc = 1 / np.sqrt(d)
+    o_ref, _ = oracle.fwd(qn, kn, vn, causal)
+    pk_ref, _ = oracle.fwd(qn, kn, kn, causal)  # sum_j P_ij K_j
+    dD = 2.0 ** -9 * np.abs(dn * o_ref).sum(-1)
+    dq_bound = TOL[torch.bfloat16] + sc * float(dD.max()) * float(np.abs(pk_ref).max())
+    refs = oracle.bwd(qn, kn, vn, dn, causal)
+    dq32, dk32, dv32 = res["g32"]
+    assert_close_f32(dv32, refs[2], torch.bfloat16, what + " dV")
+    assert_close_f32(dk32, refs[1], torch.bfloat16, what + " dK")
+    err = float(np.abs(to_np(dq32) - refs[0]).max())
+    assert err <= dq_bound, f"{what} dQ: {err:.3e} > derived bound {dq_bound:.3e}"
 
 
 def test_mha_f16_workload_full(dev):
@@ -166,11 +183,16 @@ def test_long_context_bf16_workload_sampled(dev):
         assert_close_f32(dq32[rows[:8, 0], rows[:8, 1], rows[:8, 2]], dq_r, torch.bfloat16, f"long dQ g={g}")
         assert_close_f32(dk32[0, 0, keys[:, 2]], dk_r, torch.bfloat16, f"long dK g={g}")
         assert_close_f32(dv32[0, 0, keys[:, 2]], dv_r, torch.bfloat16, f"long dV g={g}")
-    dk32 = res["g32"][1].double()
-    dv32 = res["g32"][2].double()
-    assert float(dk32.sum(dim=2).abs().max()) < 0.05
+    # Properties over all 32768 keys.  Rounding leaves sum_j dK_j a small fraction of the
+    # size a sum of unrelated terms would have (sqrt(sum_j dK_j^2)); without the property the
+    # ratio would be of order 1.  Likewise sum_j dV_j against the sum of dO rows.
+    dk32 = res["g32"][1].double().cpu()
+    dv32 = res["g32"][2].double().cpu()
+    ratio = dk32.sum(dim=2).abs() / dk32.pow(2).sum(dim=2).sqrt()
+    assert float(ratio.max()) < 0.1, float(ratio.max())
     expect = dout.double().reshape(1, wl.Hkv, G, wl.N, wl.d).sum(dim=(2, 3))
-    assert float((dv32.cpu().sum(dim=2) - expect).abs().max()) < 0.5
+    rel = (dv32.sum(dim=2) - expect).abs().max() / expect.abs().max()
+    assert float(rel) < 1e-2, float(rel)
 
 
 # ------------------------------------------------------------------ varlen
