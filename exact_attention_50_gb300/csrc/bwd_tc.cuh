@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* drain = dkdv_done + 1;
   uint64_t* rows_ready = drain + 1;  // the 128 row terms (LSE, D) of the current tile are in smem
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+  const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kt = blockIdx.x;  // key tile; 0 first = the heaviest under the causal mask
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(dkdv_done, 1);
     mbar_init(drain, 1);
     mbar_init(rows_ready, kEw);
-    *abort_flag = 0;
+    abort_set(abort_flag, 0);
     mbar_init_fence();
   }
   if (warp == 8) tmem_alloc(tmem_slot, L::kTmemCols);
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         issued = it + 1;
       }
-      if (*abort_flag) {
+      if (abort_read(abort_flag)) {
         mbar_drain(kv_full, 0);
         for (int it = max(0, issued - QS); it < issued; ++it) mbar_drain(q_full + it % QS, (it / QS) & 1);
       }

@@ -14,14 +14,15 @@
 // (batch, head) or (sequence, head)), heaviest first under the causal mask.  320 threads:
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t of a group owns query
 //              row t (TMEM lane t); loads its S row, masks, updates m / l, writes P (16-bit) back
-//              over the first 64 columns of its own S row, rescales its O row when the max moved,
+//              over columns 64-127 of its own S row, rescales its O row when the max moved,
 //              and writes O / l and the LSE at the end of the item.
 //   warp 8     TMA producer (lane 0) and TMEM allocator (whole warp).
 //   warp 9     MMA issuer (lane 0).  Per key tile j, in order:
 //                PV_A(j-1) ; S_A(j) ; PV_B(j-1) ; S_B(j)
 //              so that while one group computes its softmax the tensor core works on the
-//              other tile.  S_X(j) overwrites P_X(j-1), so it is issued only after PV_X(j-1)
-//              has completed (its mbarrier), never just after it in program order.
+//              other tile.  S_X(j) is two N=64 MMAs: the half writing columns 0-63 is queued at
+//              once; the half writing columns 64-127, where P_X(j-1) lives, is issued only after
+//              PV_X(j-1) has completed (its mbarrier), never just after it in program order.
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+DP), O_B [256+DP, 256+2DP).
 // Shared memory: Q_A, Q_B, and STAGES-deep K and V rings.
 //
@@ -79,7 +80,7 @@ struct FwdLayout {
   // kLaunchRegs registers per thread; the producer warpgroup gives registers to the softmax
   // warpgroups (kRegsLow + 2 * kRegsHigh == 3 * kLaunchRegs).
   static constexpr int kThreads = 384;
-  static constexpr uint32_t kLaunchRegs = 168, kRegsLow = 72, kRegsHigh = 216;
+  static constexpr uint32_t kLaunchRegs = 168, kRegsLow = 104, kRegsHigh = 200;
   static_assert(kRegsLow + 2 * kRegsHigh == 3 * kLaunchRegs, "register split must match the launch");
 };
 
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* o_free = pv_done + 2;   // [2]
   uint64_t* drain = o_free + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+  const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(o_free + i, 128);
     }
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    abort_set(abort_flag, 0);
     mbar_init_fence();
   }
   if (warp == 8) tmem_alloc(tmem_slot, L::kTmemCols);
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         ++ic;
       }
-      if (*abort_flag) {
+      if (abort_read(abort_flag)) {
         // let the copies already issued land before the CTA's shared memory goes away
         if (ic > 0) mbar_drain(q_full, (ic - 1) & 1);
         for (uint32_t j = nk_issued > (uint32_t)S ? nk_issued - S : 0; j < nk_issued; ++j)
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(384, 1)
     // ================================================================ MMA issuer
     if (lane == 0) {
       constexpr bool kB = Elem<T>::kBf16;
-      constexpr uint32_t idS = idesc_f16(kB, false, false, 128, kBN);
+      constexpr uint32_t idS = idesc_f16(kB, false, false, 128, kBN / 2);
       constexpr uint32_t idO = idesc_f16(kB, false, true, 128, DP);
       const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
       uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
@@ -264,16 +265,24 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t dQ = smem_desc_sw128(aQ, 16, 1024);
       const uint64_t dK = smem_desc_sw128(aK, 16, 1024);
       const uint64_t dV = smem_desc_sw128(aV, L::kChunkBytes, 1024);
+      // S_x(t) in two N=64 halves: keys 0-63 -> columns 0-63 go at once (P_x(t-1) lives in
+      // columns 64-127); keys 64-127 -> columns 64-127 wait until PV_x(t-1) has read P_x(t-1).
       auto issue_s = [&](int x, uint32_t t) -> bool {
-        // S_x for global tile t: P_x of tile t-1 must have been consumed by PV_x(t-1)
-        if (t > 0 && !mbar_wait(pv_done + x, (t - 1) & 1, abort_flag, p.status)) return false;
-        tc_fence_after();
         const uint64_t qx = dQ + ((x * L::kTileBytes) >> 4);
         const uint64_t kx = dK + (((t % S) * L::kTileBytes) >> 4);
+        tc_fence_after();
 #pragma unroll 1
-        for (int ks = 0; ks < DP / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + x * 128, qx + off, kx + off, idS, ks > 0 ? 1u : 0u);
+        for (int half = 0; half < 2; ++half) {
+          if (half == 1) {
+            if (t > 0 && !mbar_wait(pv_done + x, (t - 1) & 1, abort_flag, p.status)) return false;
+            tc_fence_after();
+          }
+          const uint64_t kh = kx + ((half * 64 * 128) >> 4);  // rows 64*half.. of the K tile
+#pragma unroll 1
+          for (int ks = 0; ks < DP / 16; ++ks) {
+            const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+            mma_ss(tmem + x * 128 + half * 64, qx + off, kh + off, idS, ks > 0 ? 1u : 0u);
+          }
         }
         mma_commit(s_full + x);
         return true;
@@ -288,7 +297,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t vx = dV + ((st * L::kTileBytes) >> 4);
 #pragma unroll 1
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          mma_ts(tO, tmem + x * 128 + ks * 8, vx + ((ks * 2048) >> 4), idO, (!first || ks > 0) ? 1u : 0u);
+          mma_ts(tO, tmem + x * 128 + 64 + ks * 8, vx + ((ks * 2048) >> 4), idO, (!first || ks > 0) ? 1u : 0u);
         }
         mma_commit(pv_done + x);
         if (last_of_pair) mma_commit(v_empty + st);
@@ -351,14 +360,23 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         float s[kBN];
         {
-          uint32_t r[32];
+          // all four 32-column loads in flight, one wait
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32(tS + 0, r0);
+          tmem_ld32(tS + 32, r1);
+          tmem_ld32(tS + 64, r2);
+          tmem_ld32(tS + 96, r3);
+          tmem_ld_wait();
+          tmem_reg_fence(r0);
+          tmem_reg_fence(r1);
+          tmem_reg_fence(r2);
+          tmem_reg_fence(r3);
 #pragma unroll
-          for (int c = 0; c < kBN / 32; ++c) {
-            tmem_ld32(tS + c * 32, r);
-            tmem_ld_wait();
-            tmem_reg_fence(r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) {
+            s[i] = __uint_as_float(r0[i]);
+            s[32 + i] = __uint_as_float(r1[i]);
+            s[64 + i] = __uint_as_float(r2[i]);
+            s[96 + i] = __uint_as_float(r3[i]);
           }
         }
         // keys key0 + c with c > lim are masked (past the diagonal, or past the sequence)
@@ -368,9 +386,16 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < kBN; ++c) s[c] = c > lim ? -INFINITY : s[c];
         }
-        float mx = s[0];
+        // row max with 8 independent partial maxima (short dependency chains)
+        float mp[8];
 #pragma unroll
-        for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+        for (int k = 0; k < 8; ++k) mp[k] = s[k];
+#pragma unroll
+        for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[c + k]);
+        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
         const float mx2 = mx * sl2;  // scale > 0: max commutes with the scaling
         float alpha = 1.f;
         bool resc = false;
@@ -380,20 +405,21 @@ __global__ void __launch_bounds__(384, 1)
           m = mx2;
         }
         const float mb = (m == -INFINITY) ? 0.f : m;
-        float rs = 0.f;
+        float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 partial row sums
         uint32_t pk[kBN / 2];
 #pragma unroll
         for (int c = 0; c < kBN; c += 2) {
           const float e0 = ex2_approx(fmaf(s[c], sl2, -mb));
           const float e1 = ex2_approx(fmaf(s[c + 1], sl2, -mb));
-          rs += e0 + e1;
+          sp[(c / 2) & 7] += e0 + e1;
           pk[c / 2] = Elem<T>::pack(e0, e1);
         }
+        const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         l = l * alpha + rs;
-        // P row over the first 64 columns of this row's S (keys 2c, 2c+1 in column c)
+        // P row over columns 64-127 of this row's S (keys 2c, 2c+1 in column 64 + c)
 #pragma unroll
         for (int c = 0; c < kBN / 64; ++c) {
-          tmem_st32(tS + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + c * 32));
+          tmem_st32(tS + 64 + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + c * 32));
         }
         // O_x *= alpha (after the S row is dead, to keep registers low): PV_x(t-1) has completed
         // (S_x(t) was issued after it) and PV_x(t) waits for p_full below

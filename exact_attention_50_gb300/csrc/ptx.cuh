@@ -55,20 +55,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The CTA's abort flag is a 32-bit word in shared memory, addressed through the shared window.
+__device__ __forceinline__ int abort_read(uint32_t flag) {
+  int v;
+  asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(flag) : "memory");
+  return v;
+}
+__device__ __forceinline__ void abort_set(uint32_t flag, int v) {
+  asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(flag), "r"(v) : "memory");
+}
+
 // Bounded wait for the phase with the given parity.  Returns false (after raising the abort
 // flag and, on a timeout, the device status) when the CTA must stop.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t abort_flag, unsigned* status) {
   const uint32_t b = smem_u32(bar);
   if (mbar_try_wait(b, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(b, parity)) return true;
     if ((it & 63u) == 0u) {
-      if (*abort_flag) return false;
+      if (abort_read(abort_flag)) return false;
       if (globaltimer() - t0 > kWaitTimeoutNs) {
         raise_status(status, ATTN_ERR_TIMEOUT);
-        *abort_flag = 1;
+        abort_set(abort_flag, 1);
         return false;
       }
     }

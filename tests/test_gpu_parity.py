@@ -106,22 +106,27 @@ def test_online_rescaling_under_growing_scores(dev, d, causal):
     res = gpu_fwd_bwd(q, k, v, dout, causal, None, dev)
     what = f"rescale d={d} causal={causal}"
     check_dense(res, q, k, v, dout, causal, None, torch.bfloat16, what, with_bwd=False)
-    # Backward.  D_i = dO_i . O_i uses the stored bf16 O, off by at most 2^-9 sum_c |dO_ic O_ic|
-    # (round to nearest); through dS_ij = P_ij (dP_ij - D_i) that moves dQ_i by
-    # scale * dD_i * sum_j P_ij K_j, which these large-offset keys make larger than with N(0,1)
-    # inputs.  dV does not involve D; dK gets it only through sign-mixed sums over i.
+    # Backward.  D_i = dO_i . O_i is formed from the stored bf16 O, which is off by at most
+    # 2^-8 |O_ic| (round to nearest) plus the forward's own error e_O, so
+    #   |dD_i| <= sum_c |dO_ic| (2^-8 |O_ic| + e_O).
+    # Through dS_ij = P_ij (dP_ij - D_i) that moves dQ_ic by at most scale dD_i sum_j P_ij |K_jc|
+    # and dK_jc by at most scale sum_i P_ij dD_i |Q_ic| -- exact-arithmetic consequences that
+    # these large-offset keys (|K| up to ~9) make larger than with N(0,1) inputs.  dV does not
+    # involve D and keeps the plain tolerance; dQ and dK get tolerance + that bound.
     qn, kn, vn, dn = (to_np(t) for t in (q, k, v, dout))
     sc = 1 / np.sqrt(d)
     o_ref, _ = oracle.fwd(qn, kn, vn, causal)
-    pk_ref, _ = oracle.fwd(qn, kn, kn, causal)  # sum_j P_ij K_j
-    dD = 2.0 ** -9 * np.abs(dn * o_ref).sum(-1)
-    dq_bound = TOL[torch.bfloat16] + sc * float(dD.max()) * float(np.abs(pk_ref).max())
+    e_o = float(np.abs(to_np(res["o32"]) - o_ref).max())
+    dD = (np.abs(dn) * (2.0 ** -8 * np.abs(o_ref) + e_o)).sum(-1)          # [B,H,N]
+    P = np.stack([oracle.probs(qn, kn, 0, h, causal) for h in range(H)])[None]  # [1,H,N,N]
+    bound_dq = TOL[torch.bfloat16] + sc * dD[..., None] * (P @ np.abs(kn))
+    bound_dk = TOL[torch.bfloat16] + sc * (np.swapaxes(P, -1, -2) @ (dD[..., None] * np.abs(qn)))
     refs = oracle.bwd(qn, kn, vn, dn, causal)
-    dq32, dk32, dv32 = res["g32"]
+    dq32, dk32, dv32 = (to_np(t) for t in res["g32"])
     assert_close_f32(dv32, refs[2], torch.bfloat16, what + " dV")
-    assert_close_f32(dk32, refs[1], torch.bfloat16, what + " dK")
-    err = float(np.abs(to_np(dq32) - refs[0]).max())
-    assert err <= dq_bound, f"{what} dQ: {err:.3e} > derived bound {dq_bound:.3e}"
+    for name, g, r, bnd in (("dQ", dq32, refs[0], bound_dq), ("dK", dk32, refs[1], bound_dk)):
+        excess = float((np.abs(g - r) - bnd).max())
+        assert excess <= 0, f"{what} {name}: exceeds the derived bound by {excess:.3e}"
 
 
 def test_mha_f16_workload_full(dev):
