@@ -19,9 +19,16 @@
 // by ~1e-2.  P^T hi/lo stays in TMEM (A operand of the dV MMA); dS^T hi/lo goes to shared
 // memory, where it is read K-major for dK and, as dS, MN-major for dQ.
 //
-// Warps 0-7: elementwise work, two warps per TMEM lane quadrant, each on half of the 128
-// query columns.  Warp 8: TMA producer and TMEM allocator.  Warp 9: MMA issuer.
-// dQ_t goes from TMEM into the fp32 workspace with 16-byte vector atomics.
+// 512 threads, four warpgroups with a register split:
+//   WG0, WG1  elementwise (two warps per TMEM lane quadrant, each on half of the 128 query
+//             columns): phase 1 turns S^T into P^T (hi/lo, back into TMEM), phase 2 turns dP^T
+//             into dS^T (hi/lo, into shared memory).  The next tile's LSE and D are prefetched.
+//   WG2       moves dQ_t from TMEM into the fp32 workspace (16-byte vector reductions) and
+//             writes dK, dV at the end.
+//   WG3       warp 12: TMA producer and TMEM allocator; warp 13: MMA issuer.
+// MMA order per query tile: S^T, dP^T, dV (hi, lo), dK (hi, lo), dQ (hi, lo).  The next
+// tile's S^T waits only for dV to have read P^T; its dP^T waits for the dQ readout.  Q and dO
+// have separate ring slots, released after the last MMA that reads each (dK, dV).
 #pragma once
 #include "fwd_tc.cuh"
 
@@ -40,17 +47,20 @@ struct BwdLayout {
   static constexpr int kOffdSl = kOffdSh + 2 * kChunkBytes;        // dS^T lo
   static constexpr int kOffRow = kOffdSl + 2 * kChunkBytes;        // LSE*log2e and D, 2 buffers each
   static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
-  // kv_full, q_full[QS], q_empty[QS], sdp_full, ds_full, dq_full, dq_free, dkdv_done, drain,
-  // rows_ready
-  static constexpr int kNumBars = 1 + 2 * kQStages + 7;
+  // kv_full, q_full[QS], q_empty[QS], do_full[QS], do_empty[QS], s_full, dp_full, p_full,
+  // dv_done, ds_full, ds_free, dq_full, dq_free, dkdv_done, rows_ready, drain
+  static constexpr int kNumBars = 1 + 4 * kQStages + 11;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 256 + DP;
   static constexpr uint32_t kColdQ = kColdP;
-  static constexpr int kThreads = 320;
-  static constexpr int kEwThreads = 256;  // elementwise warps 0-7
+  static constexpr int kThreads = 512;
+  static constexpr int kEwThreads = 256;  // warpgroups 0 and 1
+  // launch 128 registers per thread; 2 * kRegsEw + kRegsDq + kRegsIo == 4 * kLaunchRegs
+  static constexpr uint32_t kLaunchRegs = 128, kRegsEw = 184, kRegsDq = 88, kRegsIo = 56;
+  static_assert(2 * kRegsEw + kRegsDq + kRegsIo == 4 * kLaunchRegs, "register split must match the launch");
 };
 
 // Splits x into hi = round(x) and lo = round(x - hi) in the 16-bit type T, packed in pairs.
@@ -74,7 +84,7 @@ __device__ __forceinline__ void split_pack<__half>(float a, float b, uint32_t& h
 }
 
 template <typename T, int DP, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(512, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const BwdParams p) {
@@ -96,13 +106,19 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + QS;
-  uint64_t* sdp_full = q_empty + QS;
-  uint64_t* ds_full = sdp_full + 1;
-  uint64_t* dq_full = ds_full + 1;
+  uint64_t* do_full = q_empty + QS;
+  uint64_t* do_empty = do_full + QS;
+  uint64_t* s_full = do_empty + QS;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* p_full = dp_full + 1;
+  uint64_t* dv_done = p_full + 1;
+  uint64_t* ds_full = dv_done + 1;
+  uint64_t* ds_free = ds_full + 1;
+  uint64_t* dq_full = ds_free + 1;
   uint64_t* dq_free = dq_full + 1;
   uint64_t* dkdv_done = dq_free + 1;
-  uint64_t* drain = dkdv_done + 1;
-  uint64_t* rows_ready = drain + 1;  // the 128 row terms (LSE, D) of the current tile are in smem
+  uint64_t* rows_ready = dkdv_done + 1;  // the 128 row terms (LSE, D) of the current tile are in smem
+  uint64_t* drain = rows_ready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
@@ -120,26 +136,33 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; i < QS; ++i) {
       mbar_init(q_full + i, 1);
       mbar_init(q_empty + i, 1);
+      mbar_init(do_full + i, 1);
+      mbar_init(do_empty + i, 1);
     }
-    mbar_init(sdp_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, kEw);
+    mbar_init(dv_done, 1);
     mbar_init(ds_full, kEw);
+    mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, kEw);
+    mbar_init(dq_free, 128);
     mbar_init(dkdv_done, 1);
-    mbar_init(drain, 1);
     mbar_init(rows_ready, kEw);
+    mbar_init(drain, 1);
     abort_set(abort_flag, 0);
     mbar_init_fence();
   }
-  if (warp == 8) tmem_alloc(tmem_slot, L::kTmemCols);
+  if (warp == 12) tmem_alloc(tmem_slot, L::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
-    // ================================================================ TMA producer
-    if (lane == 0) {
+  if (warp >= 12) {
+    regs_dec<L::kRegsIo>();
+    if (warp == 12 && lane == 0) {
+      // ============================================================== TMA producer
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
@@ -149,84 +172,107 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(sK + c * L::kChunkBytes, &tmK, kv_full, c * 64, kt * kBN, b * p.Hkv + g);
         tma_load_3d(sV + c * L::kChunkBytes, &tmV, kv_full, c * 64, kt * kBN, b * p.Hkv + g);
       }
-      int issued = 0;
+      int nq_issued = 0, ndo_issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int h = g * p.G + it / per_head, qt = qt0 + it % per_head;
         const int st = it % QS;
-        if (it >= QS && !mbar_wait(q_empty + st, ((it / QS) - 1) & 1, abort_flag, p.status)) break;
-        mbar_expect_tx(q_full + st, 2 * L::kTileBytes);
-        for (int c = 0; c < kChunks; ++c) {
+        const uint32_t ph = ((it / QS) - 1) & 1;
+        // dO first: its slot frees earlier (after dV)
+        if (it >= QS && !mbar_wait(do_empty + st, ph, abort_flag, p.status)) break;
+        mbar_expect_tx(do_full + st, L::kTileBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_3d(sdO + st * L::kTileBytes + c * L::kChunkBytes, &tmdO, do_full + st, c * 64, qt * kBM,
+                      b * p.Hq + h);
+        ndo_issued = it + 1;
+        if (it >= QS && !mbar_wait(q_empty + st, ph, abort_flag, p.status)) break;
+        mbar_expect_tx(q_full + st, L::kTileBytes);
+        for (int c = 0; c < kChunks; ++c)
           tma_load_3d(sQ + st * L::kTileBytes + c * L::kChunkBytes, &tmQ, q_full + st, c * 64, qt * kBM,
                       b * p.Hq + h);
-          tma_load_3d(sdO + st * L::kTileBytes + c * L::kChunkBytes, &tmdO, q_full + st, c * 64, qt * kBM,
-                      b * p.Hq + h);
-        }
-        issued = it + 1;
+        nq_issued = it + 1;
       }
       if (abort_read(abort_flag)) {
         mbar_drain(kv_full, 0);
-        for (int it = max(0, issued - QS); it < issued; ++it) mbar_drain(q_full + it % QS, (it / QS) & 1);
+        for (int it = max(0, nq_issued - QS); it < nq_issued; ++it) mbar_drain(q_full + it % QS, (it / QS) & 1);
+        for (int it = max(0, ndo_issued - QS); it < ndo_issued; ++it)
+          mbar_drain(do_full + it % QS, (it / QS) & 1);
       }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ================================================================ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 13 && lane == 0) {
+      // ============================================================== MMA issuer
       constexpr bool kB = Elem<T>::kBf16;
       constexpr uint32_t idSS = idesc_f16(kB, false, false, 128, 128);  // S^T, dP^T
       constexpr uint32_t idKD = idesc_f16(kB, false, true, 128, DP);    // dV, dK: B MN-major
       constexpr uint32_t idQ = idesc_f16(kB, true, true, 128, DP);      // dQ: A and B MN-major
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO);
-      const uint32_t adSh = smem_u32(sdSh), adSl = smem_u32(sdSl);
+      // descriptors built once; a k-step adds its byte offset >> 4 to the start-address field
+      const uint64_t dK_k = smem_desc_sw128(smem_u32(sK), 16, 1024);               // K, K-major
+      const uint64_t dV_k = smem_desc_sw128(smem_u32(sV), 16, 1024);               // V, K-major
+      const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), L::kChunkBytes, 1024);  // K, MN-major
+      const uint64_t dQ_k = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dQ_mn = smem_desc_sw128(smem_u32(sQ), L::kChunkBytes, 1024);
+      const uint64_t ddO_k = smem_desc_sw128(smem_u32(sdO), 16, 1024);
+      const uint64_t ddO_mn = smem_desc_sw128(smem_u32(sdO), L::kChunkBytes, 1024);
+      const uint64_t dSh_k = smem_desc_sw128(smem_u32(sdSh), 16, 1024);
+      const uint64_t dSl_k = smem_desc_sw128(smem_u32(sdSl), 16, 1024);
+      const uint64_t dSh_mn = smem_desc_sw128(smem_u32(sdSh), L::kChunkBytes, 1024);
+      const uint64_t dSl_mn = smem_desc_sw128(smem_u32(sdSl), L::kChunkBytes, 1024);
+      constexpr uint32_t kStage16 = L::kTileBytes >> 4;
       bool ok = mbar_wait(kv_full, 0, abort_flag, p.status);
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % QS;
-        if (!mbar_wait(q_full + st, (it / QS) & 1, abort_flag, p.status)) { ok = false; break; }
+        const uint32_t ph = (it / QS) & 1;
+        // ---- S^T = K Q^T (needs Q and the S columns: dV of the previous tile has read P^T)
+        if (!mbar_wait(q_full + st, ph, abort_flag, p.status)) { ok = false; break; }
+        if (it >= 1 && !mbar_wait(dv_done, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int ks = 0; ks < DP / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + L::kColS, dK_k + off, dQ_k + st * kStage16 + off, idSS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        // ---- dP^T = V dO^T (needs dO and the dP columns: dQ of the previous tile read out)
+        if (!mbar_wait(do_full + st, ph, abort_flag, p.status)) { ok = false; break; }
         if (it >= 1 && !mbar_wait(dq_free, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t qbase = aQ + st * L::kTileBytes, dobase = adO + st * L::kTileBytes;
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < DP / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * L::kChunkBytes + (ks & 3) * 32;
-          mma_ss(tmem + L::kColS, smem_desc_sw128(aK + off, 16, 1024), smem_desc_sw128(qbase + off, 16, 1024),
-                 idSS, ks > 0 ? 1u : 0u);
+          const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + L::kColdP, dV_k + off, ddO_k + st * kStage16 + off, idSS, ks > 0 ? 1u : 0u);
         }
-#pragma unroll
-        for (int ks = 0; ks < DP / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * L::kChunkBytes + (ks & 3) * 32;
-          mma_ss(tmem + L::kColdP, smem_desc_sw128(aV + off, 16, 1024), smem_desc_sw128(dobase + off, 16, 1024),
-                 idSS, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(sdp_full);
-        if (!mbar_wait(ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+        mma_commit(dp_full);
+        // ---- dV += P^T dO; P^T hi/lo in TMEM: the 16 queries of k-step ks sit in the 32-column
+        // group ks/2 (hi in its first 16 columns, lo in the last 16), 8 columns per k-step
+        if (!mbar_wait(p_full, it & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        // dV += P^T dO, P^T hi then lo from TMEM: the 16 queries of k-step ks sit in the 32-column
-        // group ks/2 (hi in its first 16 columns, lo in the last 16), 8 columns per k-step.
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < kBN / 16; ++ks) {
           const uint32_t acol = L::kColS + (ks >> 1) * 32 + (ks & 1) * 8;
-          const uint64_t bd = smem_desc_sw128(dobase + ks * 2048, L::kChunkBytes, 1024);
+          const uint64_t bd = ddO_mn + st * kStage16 + ((ks * 2048) >> 4);
           mma_ts(tmem + L::kColdV, tmem + acol, bd, idKD, (it > 0 || ks > 0) ? 1u : 0u);
           mma_ts(tmem + L::kColdV, tmem + acol + 16, bd, idKD, 1u);
         }
-        // dK += dS^T Q (hi, lo)
-#pragma unroll
+        mma_commit(dv_done);
+        mma_commit(do_empty + st);
+        // ---- dK += dS^T Q (hi, lo)
+        if (!mbar_wait(ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint32_t a_off = (ks >> 2) * L::kChunkBytes + (ks & 3) * 32;
-          const uint64_t bd = smem_desc_sw128(qbase + ks * 2048, L::kChunkBytes, 1024);
-          mma_ss(tmem + L::kColdK, smem_desc_sw128(adSh + a_off, 16, 1024), bd, idKD, (it > 0 || ks > 0) ? 1u : 0u);
-          mma_ss(tmem + L::kColdK, smem_desc_sw128(adSl + a_off, 16, 1024), bd, idKD, 1u);
+          const uint32_t a_off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+          const uint64_t bd = dQ_mn + st * kStage16 + ((ks * 2048) >> 4);
+          mma_ss(tmem + L::kColdK, dSh_k + a_off, bd, idKD, (it > 0 || ks > 0) ? 1u : 0u);
+          mma_ss(tmem + L::kColdK, dSl_k + a_off, bd, idKD, 1u);
         }
-        // dQ_t = dS K (hi, lo), dS read MN-major from the dS^T tiles
-#pragma unroll
+        mma_commit(q_empty + st);
+        // ---- dQ_t = dS K (hi, lo), dS read MN-major from the dS^T tiles, into the dP columns
+#pragma unroll 1
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t bd = smem_desc_sw128(aK + ks * 2048, L::kChunkBytes, 1024);
-          mma_ss(tmem + L::kColdQ, smem_desc_sw128(adSh + ks * 2048, L::kChunkBytes, 1024), bd, idQ,
-                 ks > 0 ? 1u : 0u);
-          mma_ss(tmem + L::kColdQ, smem_desc_sw128(adSl + ks * 2048, L::kChunkBytes, 1024), bd, idQ, 1u);
+          const uint32_t off = (ks * 2048) >> 4;
+          mma_ss(tmem + L::kColdQ, dSh_mn + off, dK_mn + off, idQ, ks > 0 ? 1u : 0u);
+          mma_ss(tmem + L::kColdQ, dSl_mn + off, dK_mn + off, idQ, 1u);
         }
         mma_commit(dq_full);
-        mma_commit(q_empty + st);
+        mma_commit(ds_free);
       }
       if (ok) {
         mma_commit(dkdv_done);
@@ -236,100 +282,54 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     __syncwarp();
-  } else {
-    // ================================================================ elementwise warps 0-7
-    const int quad = warp & 3;                // TMEM lane quadrant
-    const int half = warp >> 2;               // query columns [64*half, 64*half+64)
-    const int t = quad * 32 + lane;           // TMEM lane: key row (S^T, dP^T, dK, dV), query row (dQ)
+  } else if (warp >= 8) {
+    regs_dec<L::kRegsDq>();
+    // ================================================================ dQ readout, dK/dV out
+    const int quad = warp & 3;
+    const int t = quad * 32 + lane;  // TMEM lane: query row of dQ, key row of dK / dV
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const int key = kt * kBN + t;
-    const bool key_ok = key < N;
-    const float sl2 = p.scale_log2;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int h = g * p.G + it / per_head, qt = qt0 + it % per_head;
       const size_t row_base = (static_cast<size_t>(b) * p.Hq + h) * N;
-      float* lse_buf = sLse + (it & 1) * 128;
-      float* d_buf = sD + (it & 1) * 128;
-      if (threadIdx.x < 128) {
-        const int q = qt * kBM + threadIdx.x;
-        lse_buf[threadIdx.x] = q < N ? p.lse[row_base + q] * 1.4426950408889634f : INFINITY;
-        d_buf[threadIdx.x] = q < N ? p.delta[row_base + q] : 0.f;
-      }
-      mbar_arrive(rows_ready);
-      if (!mbar_wait(rows_ready, it & 1, abort_flag, p.status)) { ok = false; break; }
-      if (!mbar_wait(sdp_full, it & 1, abort_flag, p.status)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll 1
-      for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
-        uint32_t rs[32], rd[32];
-        tmem_ld32(tl + L::kColS + cc * 32, rs);
-        tmem_ld32(tl + L::kColdP + cc * 32, rd);
-        tmem_ld_wait();
-        tmem_reg_fence(rs);
-        tmem_reg_fence(rd);
-        float pv[32], dsv[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int qi = cc * 32 + i;
-          const int q = qt * kBM + qi;
-          float pr = ex2_approx(fmaf(__uint_as_float(rs[i]), sl2, -lse_buf[qi]));
-          if (!key_ok || (CAUSAL && q < key)) pr = 0.f;
-          pv[i] = pr;
-          dsv[i] = pr * (__uint_as_float(rd[i]) - d_buf[qi]);
-        }
-        // P^T hi/lo back into the 32 S^T columns just read: hi in the first 16, lo in the last 16
-        uint32_t ph[16], pl[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) split_pack<T>(pv[2 * i], pv[2 * i + 1], ph[i], pl[i]);
-        tmem_st16(tl + L::kColS + cc * 32, ph);
-        tmem_st16(tl + L::kColS + cc * 32 + 16, pl);
-        // dS^T hi/lo -> shared memory, K-major with the 128-byte swizzle
-#pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-          const int gq = cc * 4 + gi;  // 16-byte granule index over the 128 queries
-          const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
-          uint4 a, c;
-          split_pack<T>(dsv[gi * 8 + 0], dsv[gi * 8 + 1], a.x, c.x);
-          split_pack<T>(dsv[gi * 8 + 2], dsv[gi * 8 + 3], a.y, c.y);
-          split_pack<T>(dsv[gi * 8 + 4], dsv[gi * 8 + 5], a.z, c.z);
-          split_pack<T>(dsv[gi * 8 + 6], dsv[gi * 8 + 7], a.w, c.w);
-          *reinterpret_cast<uint4*>(sdSh + off) = a;
-          *reinterpret_cast<uint4*>(sdSl + off) = c;
-        }
-      }
-      tmem_st_wait();
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(ds_full);
-      // dQ_t (lane = query row) -> fp32 workspace; this warp takes half of the d columns
       if (!mbar_wait(dq_full, it & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      {
-        const int q = qt * kBM + t;
-        float* dst = p.dq_acc + (row_base + q) * static_cast<size_t>(p.d);
-        uint32_t r[32];
+      const int q = qt * kBM + t;
+      float* dst = p.dq_acc + (row_base + q) * static_cast<size_t>(p.d);
 #pragma unroll
-        for (int c = half * (DP / 64); c < (half + 1) * (DP / 64); ++c) {
-          tmem_ld32(tl + L::kColdQ + c * 32, r);
-          tmem_ld_wait();
-          tmem_reg_fence(r);
-          if (q < N && c * 32 < p.d) {
-            const int ncol = min(32, p.d - c * 32);
+      for (int c2 = 0; c2 < DP / 64; ++c2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tl + L::kColdQ + c2 * 64, r0);
+        tmem_ld32(tl + L::kColdQ + c2 * 64 + 32, r1);
+        tmem_ld_wait();
+        tmem_reg_fence(r0);
+        tmem_reg_fence(r1);
+        if (c2 == DP / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(dq_free);  // the dQ columns may be overwritten once everything is loaded
+        }
+        if (q < N) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (i * 4 < ncol)
-                red_add_v4(dst + c * 32 + i * 4, __uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+          for (int i = 0; i < 8; ++i) {
+            const int col = c2 * 64 + i * 4;
+            if (col < p.d)
+              red_add_v4(dst + col, __uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
+                         __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int col = c2 * 64 + 32 + i * 4;
+            if (col < p.d)
+              red_add_v4(dst + col, __uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]),
+                         __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]));
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(dq_free);
     }
-    // ---- epilogue: dK (scaled) and dV rows of this key tile, half of the columns per warp
+    // ---- epilogue: dK (scaled) and dV rows of this key tile
     if (ok && mbar_wait(dkdv_done, 0, abort_flag, p.status)) {
       tc_fence_after();
+      const int key = kt * kBN + t;
       const size_t krow = (static_cast<size_t>(b) * p.Hkv + g) * N + key;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
@@ -337,22 +337,22 @@ __global__ void __launch_bounds__(320, 1)
         const float mul = which == 0 ? p.scale : 1.f;
         void* out = which == 0 ? p.dk : p.dv;
         uint32_t r[32];
-#pragma unroll
-        for (int c = half * (DP / 64); c < (half + 1) * (DP / 64); ++c) {
+#pragma unroll 1
+        for (int c = 0; c < DP / 32; ++c) {
           tmem_ld32(tl + col + c * 32, r);
           tmem_ld_wait();
           tmem_reg_fence(r);
-          if (key_ok && c * 32 < p.d) {
+          if (key < N && c * 32 < p.d) {
             const int ncol = min(32, p.d - c * 32);
             if (p.out_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + krow * p.d + c * 32);
+              float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + krow * p.d + c * 32);
 #pragma unroll
               for (int i = 0; i < 8; ++i)
                 if (i * 4 < ncol)
-                  dst[i] = make_float4(__uint_as_float(r[4 * i]) * mul, __uint_as_float(r[4 * i + 1]) * mul,
-                                       __uint_as_float(r[4 * i + 2]) * mul, __uint_as_float(r[4 * i + 3]) * mul);
+                  o4[i] = make_float4(__uint_as_float(r[4 * i]) * mul, __uint_as_float(r[4 * i + 1]) * mul,
+                                      __uint_as_float(r[4 * i + 2]) * mul, __uint_as_float(r[4 * i + 3]) * mul);
             } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(out) + krow * p.d + c * 32);
+              uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(out) + krow * p.d + c * 32);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 if (i * 8 < ncol) {
@@ -361,18 +361,116 @@ __global__ void __launch_bounds__(320, 1)
                   v.y = Elem<T>::pack(__uint_as_float(r[8 * i + 2]) * mul, __uint_as_float(r[8 * i + 3]) * mul);
                   v.z = Elem<T>::pack(__uint_as_float(r[8 * i + 4]) * mul, __uint_as_float(r[8 * i + 5]) * mul);
                   v.w = Elem<T>::pack(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul);
-                  dst[i] = v;
+                  o4[i] = v;
                 }
             }
           }
         }
       }
     }
+  } else {
+    regs_inc<L::kRegsEw>();
+    // ================================================================ elementwise warps 0-7
+    const int quad = warp & 3;                // TMEM lane quadrant
+    const int half = warp >> 2;               // query columns [64*half, 64*half+64)
+    const int t = quad * 32 + lane;           // TMEM lane: key row
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int key = kt * kBN + t;
+    const bool key_ok = key < N;
+    const float sl2 = p.scale_log2;
+    // row terms of tile `it`, loaded one tile ahead by threads 0..127
+    float lse_next = 0.f, d_next = 0.f;
+    auto load_rows = [&](int it) {
+      if (threadIdx.x < 128 && it < n_it) {
+        const int h = g * p.G + it / per_head, qt = qt0 + it % per_head;
+        const size_t row_base = (static_cast<size_t>(b) * p.Hq + h) * N;
+        const int q = qt * kBM + threadIdx.x;
+        lse_next = q < N ? p.lse[row_base + q] * 1.4426950408889634f : INFINITY;
+        d_next = q < N ? p.delta[row_base + q] : 0.f;
+      }
+    };
+    load_rows(0);
+    for (int it = 0; it < n_it; ++it) {
+      const int qt = qt0 + it % per_head;
+      float* lse_buf = sLse + (it & 1) * 128;
+      float* d_buf = sD + (it & 1) * 128;
+      if (threadIdx.x < 128) {
+        lse_buf[threadIdx.x] = lse_next;
+        d_buf[threadIdx.x] = d_next;
+      }
+      mbar_arrive(rows_ready);
+      if (!mbar_wait(rows_ready, it & 1, abort_flag, p.status)) break;
+      // ---- phase 1: P^T = exp2(S^T * scale * log2e - LSE * log2e), hi/lo back into TMEM
+      if (!mbar_wait(s_full, it & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      float pv[64];
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tl + L::kColS + half * 64, r0);
+        tmem_ld32(tl + L::kColS + half * 64 + 32, r1);
+        tmem_ld_wait();
+        tmem_reg_fence(r0);
+        tmem_reg_fence(r1);
+        // queries q < key are masked under causal: only the diagonal tile has any
+        const int lim = CAUSAL ? key - qt * kBM - half * 64 : -1;  // columns c < lim are masked
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const uint32_t raw = i < 32 ? r0[i] : r1[i - 32];
+          float pr = ex2_approx(fmaf(__uint_as_float(raw), sl2, -lse_buf[half * 64 + i]));
+          if (i < lim) pr = 0.f;
+          pv[i] = key_ok ? pr : 0.f;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t ph[16], pl[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) split_pack<T>(pv[cc * 32 + 2 * i], pv[cc * 32 + 2 * i + 1], ph[i], pl[i]);
+          tmem_st16(tl + L::kColS + half * 64 + cc * 32, ph);
+          tmem_st16(tl + L::kColS + half * 64 + cc * 32 + 16, pl);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(p_full);
+      load_rows(it + 1);  // prefetch the next tile's LSE and D
+      // ---- phase 2: dS^T = P^T (dP^T - D), hi/lo into shared memory
+      if (it >= 1 && !mbar_wait(ds_free, (it - 1) & 1, abort_flag, p.status)) break;
+      if (!mbar_wait(dp_full, it & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tl + L::kColdP + half * 64, r0);
+        tmem_ld32(tl + L::kColdP + half * 64 + 32, r1);
+        tmem_ld_wait();
+        tmem_reg_fence(r0);
+        tmem_reg_fence(r1);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const uint32_t raw = i < 32 ? r0[i] : r1[i - 32];
+          pv[i] = pv[i] * (__uint_as_float(raw) - d_buf[half * 64 + i]);
+        }
+      }
+      tc_fence_before();  // the dP columns are consumed (the dQ MMA may overwrite them)
+#pragma unroll
+      for (int gi = 0; gi < 8; ++gi) {
+        const int gq = half * 8 + gi;  // 16-byte granule index over the 128 queries
+        const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
+        uint4 a, c;
+        split_pack<T>(pv[gi * 8 + 0], pv[gi * 8 + 1], a.x, c.x);
+        split_pack<T>(pv[gi * 8 + 2], pv[gi * 8 + 3], a.y, c.y);
+        split_pack<T>(pv[gi * 8 + 4], pv[gi * 8 + 5], a.z, c.z);
+        split_pack<T>(pv[gi * 8 + 6], pv[gi * 8 + 7], a.w, c.w);
+        *reinterpret_cast<uint4*>(sdSh + off) = a;
+        *reinterpret_cast<uint4*>(sdSl + off) = c;
+      }
+      fence_async_smem();
+      mbar_arrive(ds_full);
+    }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -384,6 +482,11 @@ cudaError_t launch_bwd_tc_t(const BwdMaps& maps, const BwdParams& p, cudaStream_
   auto kern = bwd_tc_kernel<T, DP, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
+  // The in-kernel register split assumes the launch allocation; never launch otherwise.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != static_cast<int>(L::kLaunchRegs)) return cudaErrorInvalidConfiguration;
   const dim3 grid(p.n_ktiles, p.B * p.Hkv);
   kern<<<grid, L::kThreads, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, maps.dout, p);
   return cudaGetLastError();
