@@ -54,6 +54,8 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_main.restype = i
         lib.attn_bwd_finish.argtypes = [vp, vp, ctypes.c_size_t, i, i, i, i, f, i, u, vp]
         lib.attn_bwd_finish.restype = i
+        lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, u, vp]
+        lib.attn_bwd_noalloc.restype = i
         lib.attn_get_device_status.argtypes = [vp]
         lib.attn_get_device_status.restype = i
         lib.attn_status_string.argtypes = [i]
@@ -104,6 +106,13 @@ def attn_bwd_main(q, k, v, dout, lse, dq, dk, dv, workspace, workspace_bytes, B,
 
 def attn_bwd_finish(dq, workspace, workspace_bytes, B, Hq, N, d, scale, dtype, flags, stream) -> int:
     return load().attn_bwd_finish(dq, workspace, workspace_bytes, B, Hq, N, d, float(scale), dtype, flags, stream)
+
+
+def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype, flags,
+                     stream) -> int:
+    """attn_bwd without a caller workspace (a fixed 64 MiB scratch array inside the library)."""
+    return load().attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, int(causal), float(scale),
+                                   dtype, flags, stream)
 
 
 def attn_get_device_status(stream) -> int:

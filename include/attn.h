@@ -128,6 +128,28 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
 attn_status_t attn_bwd_finish(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int N, int d,
                               float scale, attn_dtype_t dtype, unsigned flags, void* stream);
 
+/*
+ * attn_bwd_noalloc -- the backward (same arguments, layouts and results as attn_bwd) for callers
+ * that cannot allocate device memory when they call it: for example a plugin or host program
+ * whose GPU memory is reserved up front by another allocator and may not grow on its hot path,
+ * or a runtime that forbids allocation calls after start-up.  The pages describe no such call;
+ * it exists only for such callers.
+ *   - Scratch comes from a fixed 64 MiB array inside this library (not from the caller and not
+ *     from any allocator).  Every GPU that loads the library holds that array until the process
+ *     exits.  No call on this path allocates or frees device memory.
+ *   - Sizes are limited by it: when attn_bwd_workspace_bytes(B, Hq, N, d) exceeds 64 MiB
+ *     (67108864 bytes; at d = 128 that is about 127,000 query rows B*Hq*N) the call returns
+ *     ATTN_ERR_UNSUPPORTED and launches nothing.
+ *   - The first call on each device looks up the array's device address (a one-time set-up on
+ *     that device, made while it is current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents; each call clears the
+ *     part that must start at zero itself.  Calls whose execution overlaps on the GPU (other
+ *     streams, or other host threads) race on the array and give wrong results: order them.
+ */
+attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                               int d, int causal, float scale, attn_dtype_t dtype, unsigned flags, void* stream);
+
 /* Synchronises `stream`, then returns and clears the first error the current device's
  * kernels recorded (ATTN_OK when none).  Returns ATTN_ERR_CUDA if the synchronisation fails. */
 attn_status_t attn_get_device_status(void* stream);
