@@ -1,5 +1,5 @@
-// fwd_tc.cuh -- tcgen05 forward for fp16 / bf16: persistent, TMA-fed, warp-specialised, two
-// 128-row query tiles per CTA sharing every K/V tile, S / P / O in TMEM.
+// fwd_tc.cuh -- tcgen05 forward for fp16 / bf16: persistent, TMA-fed, warp-specialised, S / P / O
+// in TMEM.
 //
 // What it computes (per query row i of a (batch, head) or (sequence, head)):
 //   S_ij = scale * Q_i . K_j, masked to -inf for j > i (causal) and for keys past the sequence;
@@ -10,27 +10,22 @@
 // The online max/sum update follows the FlashAttention-T review, best practice 4; scale and
 // mask are applied inside the GEMM loop as in its best practice 2.
 //
-// A CTA loops over work items (a pair of consecutive 128-row query tiles A and B of one
-// (batch, head) or (sequence, head)), heaviest first under the causal mask.  320 threads:
-//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: thread t of a group owns query
-//              row t (TMEM lane t); loads its S row, masks, updates m / l, writes P (16-bit) back
-//              over columns 64-127 of its own S row, rescales its O row when the max moved,
-//              and writes O / l and the LSE at the end of the item.
+// A CTA loops over 128-row query tiles (heaviest first under the causal mask).  320 threads:
+//   warps 0-3  softmax, key columns 0-63 of each S tile; warps 4-7 softmax, key columns 64-127.
+//              Thread t of either group owns query row t (TMEM lane t).  The two threads of a
+//              row exchange their partial row maxima through shared memory, so both use the
+//              same running max; each keeps its own partial row sum, combined at the end.  Each
+//              writes its 64 P values (16-bit) back over the first half of the S tile's columns,
+//              rescales its half of the O row when the max moved, and writes that half of O.
 //   warp 8     TMA producer (lane 0) and TMEM allocator (whole warp).
-//   warp 9     MMA issuer (lane 0).  Per key tile j, in order:
-//                PV_A(j-1) ; S_A(j) ; PV_B(j-1) ; S_B(j)
-//              so that while one group computes its softmax the tensor core works on the
-//              other tile.  S_X(j) is two N=64 MMAs: the half writing columns 0-63 is queued at
-//              once; the half writing columns 64-127, where P_X(j-1) lives, is issued only after
-//              PV_X(j-1) has completed (its mbarrier), never just after it in program order.
-// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+DP), O_B [256+DP, 256+2DP).
-// Shared memory: Q_A, Q_B, and STAGES-deep K and V rings.
+//   warp 9     MMA issuer (lane 0): a non-blocking scheduler over the streams S(j) and PV(j).
+// TMEM: S double buffer at columns [0,128) and [128,256), O at [256, 256+DP).  S(j) goes into
+// buffer j % 2, where P(j-2) lives, so it waits only for PV(j-2) -- long finished -- and the
+// tensor core computes S(j+1) while the softmax works on S(j).
 //
 // Lazy rescaling: the running max used for the exponentials is only moved when a tile's max
 // exceeds it by more than kRescaleLog2 (log2 units); the final O / l and LSE use the same max,
-// so the result is exact, and P stays below 2^kRescaleLog2 (well inside fp16 range).  Because
-// S_X(j) is issued after PV_X(j-1) completed, a softmax group that sees S_X(j) may rescale O_X
-// at once.
+// so the result is exact, and P stays below 2^kRescaleLog2 (well inside fp16 range).
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -65,23 +60,19 @@ struct FwdLayout {
   static constexpr int kStages = DP == 128 ? 2 : 4;
   static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 64 elements x 2 B
   static constexpr int kTileBytes = (DP / 64) * kChunkBytes;
-  static constexpr int kOffQ = 0;                        // Q_A then Q_B
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffX = kOffV + kStages * kTileBytes;  // exchange [2 slots][2 groups][128 rows]
+  static constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
   // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-  // pv_done[2], o_free[2], drain
-  static constexpr int kNumBars = 2 + 4 * kStages + 8 + 1;
+  // pv_done[2], o_free, xch[2], drain
+  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 1 + 2 + 1;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base (u32), abort flag (int)
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;         // slack for 1024-byte alignment
   static constexpr uint32_t kTmemCols = 512;
-  // 3 warpgroups: softmax A, softmax B, and producer / MMA (+2 idle warps).  Launched at
-  // kLaunchRegs registers per thread; the producer warpgroup gives registers to the softmax
-  // warpgroups (kRegsLow + 2 * kRegsHigh == 3 * kLaunchRegs).
-  static constexpr int kThreads = 384;
-  static constexpr uint32_t kLaunchRegs = 168, kRegsLow = 104, kRegsHigh = 200;
-  static_assert(kRegsLow + 2 * kRegsHigh == 3 * kLaunchRegs, "register split must match the launch");
+  static constexpr int kThreads = 320;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -90,9 +81,9 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>(a + ((1024u - (s & 1023u)) & 1023u));
 }
 
-// One work item: a pair of 128-row query tiles (rows [256*pair, 256*pair+256) of a sequence).
+// One work item: a 128-row query tile of one (batch, head) or (sequence, head).
 struct FwdItem {
-  int b, h, pair, seq_start, seq_len, n_kv;
+  int b, h, qt, seq_start, seq_len, n_kv;
   bool valid;
 };
 
@@ -100,9 +91,9 @@ template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int idx) {
   FwdItem it;
   const int heads = VARLEN ? p.Hq : p.B * p.Hq;
-  const int per_pair = VARLEN ? heads * p.nseq : heads;
-  it.pair = p.n_qtiles - 1 - idx / per_pair;  // n_qtiles counts pairs here; heaviest first
-  const int rem = idx % per_pair;
+  const int per_tile = VARLEN ? heads * p.nseq : heads;
+  it.qt = p.n_qtiles - 1 - idx / per_tile;  // heaviest first
+  const int rem = idx % per_tile;
   it.valid = true;
   if constexpr (VARLEN) {
     const int s = rem / heads;
@@ -112,12 +103,12 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int idx) {
     const bool bad = c0 < 0 || c1 < c0 || c1 > p.total_tokens || c1 - c0 > p.max_seqlen ||
                      (s == 0 && c0 != 0) || (s == p.nseq - 1 && c1 != p.total_tokens);
     if (bad) {
-      if (it.pair == 0 && it.h == 0) raise_status(p.status, ATTN_ERR_DEVICE_INPUT);
+      if (it.qt == 0 && it.h == 0) raise_status(p.status, ATTN_ERR_DEVICE_INPUT);
       it.valid = false;
     }
     it.seq_start = c0;
     it.seq_len = c1 - c0;
-    if (it.pair * 2 * kBM >= it.seq_len) it.valid = false;
+    if (it.qt * kBM >= it.seq_len) it.valid = false;
   } else {
     it.b = rem / p.Hq;
     it.h = rem % p.Hq;
@@ -125,13 +116,13 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int idx) {
     it.seq_len = p.N;
   }
   const int n_kv_all = (it.seq_len + kBN - 1) / kBN;
-  it.n_kv = CAUSAL ? min(2 * it.pair + 2, n_kv_all) : n_kv_all;
+  it.n_kv = CAUSAL ? min(it.qt + 1, n_kv_all) : n_kv_all;
   if (it.n_kv <= 0) it.valid = false;
   return it;
 }
 
 template <typename T, int DP, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(320, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p, int n_items) {
   using L = FwdLayout<DP>;
@@ -142,6 +133,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sQ = smem + L::kOffQ;
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
+  float* sX = reinterpret_cast<float*>(smem + L::kOffX);  // [slot][group][row]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
@@ -149,11 +141,14 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* k_empty = k_full + S;
   uint64_t* v_full = k_empty + S;
   uint64_t* v_empty = v_full + S;
-  uint64_t* s_full = v_empty + S;   // [2]: tile A, tile B
-  uint64_t* p_full = s_full + 2;    // [2]
-  uint64_t* pv_done = p_full + 2;   // [2]
-  uint64_t* o_free = pv_done + 2;   // [2]
-  uint64_t* drain = o_free + 2;
+  // Per S buffer b: s_full (S(j) ready), p_full (P(j) written over it), pv_done (PV(j) done),
+  // for the tiles j with j % 2 == b; phase k of each is tile 2k + b.
+  uint64_t* s_full = v_empty + S;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* o_free = pv_done + 2;
+  uint64_t* xch = o_free + 1;       // [2]: row-max / row-sum exchange slots
+  uint64_t* drain = xch + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
@@ -170,10 +165,11 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 128);
+      mbar_init(p_full + i, 256);
       mbar_init(pv_done + i, 1);
-      mbar_init(o_free + i, 128);
+      mbar_init(xch + i, 256);
     }
+    mbar_init(o_free, 256);
     mbar_init(drain, 1);
     abort_set(abort_flag, 0);
     mbar_init_fence();
@@ -183,12 +179,8 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Each register-budget change opens its own branch, which runs to the teardown.
-  if (warp >= 8) {
-  regs_dec<L::kRegsLow>();
-  if (warp >= 10) {
-    // spare warps of the producer warpgroup: nothing to do
-  } else if (warp == 8) {
+
+  if (warp == 8) {
     // ================================================================ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -202,16 +194,13 @@ __global__ void __launch_bounds__(384, 1)
         const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
         if (!it.valid) continue;
         if (ic > 0 && !mbar_wait(q_empty, (ic - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        mbar_expect_tx(q_full, 2 * L::kTileBytes);
-        for (int x = 0; x < 2; ++x) {
-          const int row0 = (2 * it.pair + x) * kBM;
-          for (int c = 0; c < kChunks; ++c) {
-            uint8_t* dst = sQ + x * L::kTileBytes + c * L::kChunkBytes;
-            if constexpr (VARLEN)
-              tma_load_4d(dst, &tmQ, q_full, c * 64, it.h, 0, it.seq_start + row0);
-            else
-              tma_load_3d(dst, &tmQ, q_full, c * 64, row0, it.b * p.Hq + it.h);
-          }
+        mbar_expect_tx(q_full, L::kTileBytes);
+        for (int c = 0; c < kChunks; ++c) {
+          uint8_t* dst = sQ + c * L::kChunkBytes;
+          if constexpr (VARLEN)
+            tma_load_4d(dst, &tmQ, q_full, c * 64, it.h, 0, it.seq_start + it.qt * kBM);
+          else
+            tma_load_3d(dst, &tmQ, q_full, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
         }
         const int g = it.h / p.G;
         for (int j = 0; j < it.n_kv; ++j, ++kv) {
@@ -254,82 +243,87 @@ __global__ void __launch_bounds__(384, 1)
     // ================================================================ MMA issuer
     if (lane == 0) {
       constexpr bool kB = Elem<T>::kBf16;
-      constexpr uint32_t idS = idesc_f16(kB, false, false, 128, kBN / 2);
+      constexpr uint32_t idS = idesc_f16(kB, false, false, 128, kBN);
       constexpr uint32_t idO = idesc_f16(kB, false, true, 128, DP);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      // Descriptors are built once; a k-step adds its byte offset >> 4 to the start-address
+      // field (shared addresses stay below 256 KB, so the 14-bit field never carries).
+      const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = smem_desc_sw128(smem_u32(sV), L::kChunkBytes, 1024);
       uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
       uint32_t ic = 0;
       bool ok = true;
-      // Descriptors are built once; a k-step adds its byte offset >> 4 to the start-address
-      // field (shared addresses stay below 256 KB, so the 14-bit field never carries).
-      const uint64_t dQ = smem_desc_sw128(aQ, 16, 1024);
-      const uint64_t dK = smem_desc_sw128(aK, 16, 1024);
-      const uint64_t dV = smem_desc_sw128(aV, L::kChunkBytes, 1024);
-      // S_x(t) in two N=64 halves: keys 0-63 -> columns 0-63 go at once (P_x(t-1) lives in
-      // columns 64-127); keys 64-127 -> columns 64-127 wait until PV_x(t-1) has read P_x(t-1).
-      auto issue_s = [&](int x, uint32_t t) -> bool {
-        const uint64_t qx = dQ + ((x * L::kTileBytes) >> 4);
+      auto issue_s = [&](uint32_t t) {
         const uint64_t kx = dK + (((t % S) * L::kTileBytes) >> 4);
         tc_fence_after();
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          if (half == 1) {
-            if (t > 0 && !mbar_wait(pv_done + x, (t - 1) & 1, abort_flag, p.status)) return false;
-            tc_fence_after();
-          }
-          const uint64_t kh = kx + ((half * 64 * 128) >> 4);  // rows 64*half.. of the K tile
-#pragma unroll 1
-          for (int ks = 0; ks < DP / 16; ++ks) {
-            const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-            mma_ss(tmem + x * 128 + half * 64, qx + off, kh + off, idS, ks > 0 ? 1u : 0u);
-          }
+        for (int ks = 0; ks < DP / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + (t & 1) * 128, dQ + off, kx + off, idS, ks > 0 ? 1u : 0u);
         }
-        mma_commit(s_full + x);
-        return true;
+        mma_commit(s_full + (t & 1));
       };
-      auto issue_pv = [&](int x, uint32_t t, bool first, bool last_of_pair) -> bool {
-        if (!mbar_wait(p_full + x, t & 1, abort_flag, p.status)) return false;
-        if (first && ic > 0 && !mbar_wait(o_free + x, (ic - 1) & 1, abort_flag, p.status)) return false;
-        const int st = t % S;
-        if (!mbar_wait(v_full + st, (t / S) & 1, abort_flag, p.status)) return false;
+      auto issue_pv = [&](uint32_t t, bool first) {
         tc_fence_after();
-        const uint32_t tO = tmem + 256 + x * DP;
-        const uint64_t vx = dV + ((st * L::kTileBytes) >> 4);
+        const uint64_t vx = dV + (((t % S) * L::kTileBytes) >> 4);
+        // P(t) over columns [0,64) of S buffer t % 2: keys 2c, 2c+1 in column c
 #pragma unroll 1
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          mma_ts(tO, tmem + x * 128 + 64 + ks * 8, vx + ((ks * 2048) >> 4), idO, (!first || ks > 0) ? 1u : 0u);
-        }
-        mma_commit(pv_done + x);
-        if (last_of_pair) mma_commit(v_empty + st);
-        return true;
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          mma_ts(tmem + 256, tmem + (t & 1) * 128 + ks * 8, vx + ((ks * 2048) >> 4), idO,
+                 (!first || ks > 0) ? 1u : 0u);
+        mma_commit(pv_done + (t & 1));
+        mma_commit(v_empty + t % S);
       };
+      // A small scheduler over the two streams, polled without blocking:
+      //   S(j)  needs Q, K_j, and PV(j-2) complete (S(j) overwrites P(j-2) in buffer j % 2);
+      //   PV(j) needs P(j) (p_full) and V_j, and for an item's first tile the previous item's O
+      //         read out (o_free).
+      // K_j is released once S(j) is issued, Q once the item's last S is.  Every barrier tested
+      // here cannot complete its next phase before this thread issues something, so a phase is
+      // never skipped between two polls.
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
         const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
         if (!it.valid) continue;
-        if (!mbar_wait(q_full, ic & 1, abort_flag, p.status)) { ok = false; break; }
+        const int n = it.n_kv;
         const uint32_t t0 = kv;
-        // prologue: S_A(0), S_B(0)
-        if (!mbar_wait(k_full + t0 % S, (t0 / S) & 1, abort_flag, p.status)) { ok = false; break; }
-        if (!issue_s(0, t0) || !issue_s(1, t0)) { ok = false; break; }
-        mma_commit(k_empty + t0 % S);
-        if (it.n_kv == 1) mma_commit(q_empty);  // the item's last MMA reading Q_A / Q_B is issued
-        for (int j = 0; j < it.n_kv; ++j) {
-          const uint32_t t = t0 + j;
-          const bool more = j + 1 < it.n_kv;
-          if (!issue_pv(0, t, j == 0, false)) { ok = false; break; }
-          if (more) {
-            if (!mbar_wait(k_full + (t + 1) % S, ((t + 1) / S) & 1, abort_flag, p.status)) { ok = false; break; }
-            if (!issue_s(0, t + 1)) { ok = false; break; }
+        int ns = 0, np = 0;
+        bool q_ready = false;
+        unsigned long long t_idle = 0;
+        while (np < n) {
+          bool progress = false;
+          if (!q_ready) q_ready = mbar_test(q_full, ic & 1);
+          const uint32_t ts = t0 + ns;
+          if (q_ready && ns < n && ns <= np + 1 && mbar_test(k_full + ts % S, (ts / S) & 1) &&
+              (ts < 2 || mbar_test(pv_done + (ts & 1), ((ts - 2) >> 1) & 1))) {
+            issue_s(ts);
+            mma_commit(k_empty + ts % S);
+            ++ns;
+            if (ns == n) mma_commit(q_empty);
+            progress = true;
           }
-          if (!issue_pv(1, t, j == 0, true)) { ok = false; break; }
-          if (more) {
-            if (!issue_s(1, t + 1)) { ok = false; break; }
-            mma_commit(k_empty + (t + 1) % S);
-            if (j + 2 == it.n_kv) mma_commit(q_empty);  // last MMA reading Q_A / Q_B issued
+          const uint32_t tp = t0 + np;
+          if (np < ns && mbar_test(p_full + (tp & 1), (tp >> 1) & 1) && mbar_test(v_full + tp % S, (tp / S) & 1) &&
+              (np > 0 || ic == 0 || mbar_test(o_free, (ic - 1) & 1))) {
+            issue_pv(tp, np == 0);
+            ++np;
+            progress = true;
+          }
+          if (progress) {
+            t_idle = 0;
+          } else {
+            const unsigned long long now = globaltimer();
+            if (t_idle == 0) t_idle = now;
+            if (abort_read(abort_flag)) { ok = false; break; }
+            if (now - t_idle > kWaitTimeoutNs) {
+              raise_status(p.status, ATTN_ERR_TIMEOUT);
+              abort_set(abort_flag, 1);
+              ok = false;
+              break;
+            }
           }
         }
         if (!ok) break;
-        kv = t0 + it.n_kv;
+        kv = t0 + n;
         ++ic;
       }
       if (!ok) {
@@ -338,64 +332,73 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
     __syncwarp();
-  }
   } else {
-    regs_inc<L::kRegsHigh>();
     // ================================================================ softmax groups
-    const int x = warp >> 2;                  // 0 = tile A, 1 = tile B
+    const int grp = warp >> 2;                // 0: key columns 0-63, 1: key columns 64-127
     const int row = threadIdx.x & 127;        // TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t tS = tl + x * 128, tO = tl + 256 + x * DP;
+    const uint32_t tO = tl + 256 + grp * (DP / 2);  // this group's half of the O row
     const float sl2 = p.scale_log2;
     uint32_t kv = 0, ic = 0;
+    uint32_t xc = 0;  // exchanges done (slot xc % 2, phase (xc / 2) % 2)
     bool ok = true;
+    // Writes this thread's value to the exchange slot and returns the other group's value.
+    auto exchange = [&](float v, float& other) -> bool {
+      float* xb = sX + (xc & 1) * 256;
+      xb[grp * 128 + row] = v;
+      tc_fence_before();  // also orders this thread's S reads before the other group's P writes
+      mbar_arrive(xch + (xc & 1));
+      if (!mbar_wait(xch + (xc & 1), (xc >> 1) & 1, abort_flag, p.status)) return false;
+      tc_fence_after();
+      other = xb[(grp ^ 1) * 128 + row];
+      ++xc;
+      return true;
+    };
     for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
       const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
       if (!it.valid) continue;
-      const int q_row = (2 * it.pair + x) * kBM + row;  // relative to the sequence
-      float m = -INFINITY, l = 0.f;
+      const int q_row = it.qt * kBM + row;  // relative to the sequence
+      float m = -INFINITY, l = 0.f;          // l: this group's partial row sum
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t t = kv + j;
-        if (!mbar_wait(s_full + x, t & 1, abort_flag, p.status)) { ok = false; break; }
+        const int b = t & 1;
+        if (!mbar_wait(s_full + b, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        float s[kBN];
+        const uint32_t tS = tl + b * 128;
+        float s[64];
         {
-          // all four 32-column loads in flight, one wait
-          uint32_t r0[32], r1[32], r2[32], r3[32];
-          tmem_ld32(tS + 0, r0);
-          tmem_ld32(tS + 32, r1);
-          tmem_ld32(tS + 64, r2);
-          tmem_ld32(tS + 96, r3);
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tS + grp * 64, r0);
+          tmem_ld32(tS + grp * 64 + 32, r1);
           tmem_ld_wait();
           tmem_reg_fence(r0);
           tmem_reg_fence(r1);
-          tmem_reg_fence(r2);
-          tmem_reg_fence(r3);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             s[i] = __uint_as_float(r0[i]);
             s[32 + i] = __uint_as_float(r1[i]);
-            s[64 + i] = __uint_as_float(r2[i]);
-            s[96 + i] = __uint_as_float(r3[i]);
           }
         }
         // keys key0 + c with c > lim are masked (past the diagonal, or past the sequence)
-        const int key0 = j * kBN;
+        const int key0 = j * kBN + grp * 64;
         const int lim = CAUSAL ? min(q_row, it.seq_len - 1) - key0 : it.seq_len - 1 - key0;
-        if (lim < kBN - 1) {
+        if (lim < 63) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) s[c] = c > lim ? -INFINITY : s[c];
+          for (int c = 0; c < 64; ++c) s[c] = c > lim ? -INFINITY : s[c];
         }
-        // row max with 8 independent partial maxima (short dependency chains)
+        // partial row max with 8 independent chains, then the other group's
         float mp[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mp[k] = s[k];
 #pragma unroll
-        for (int c = 8; c < kBN; c += 8)
+        for (int c = 8; c < 64; c += 8)
 #pragma unroll
           for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[c + k]);
-        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                         fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        float mo;
+        if (!exchange(mx, mo)) { ok = false; break; }
+        mx = fmaxf(mx, mo);
         const float mx2 = mx * sl2;  // scale > 0: max commutes with the scaling
         float alpha = 1.f;
         bool resc = false;
@@ -406,28 +409,40 @@ __global__ void __launch_bounds__(384, 1)
         }
         const float mb = (m == -INFINITY) ? 0.f : m;
         float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 partial row sums
-        uint32_t pk[kBN / 2];
+        uint32_t pk[32];
+        // In tiles with no masked key a quarter of the exponentials run on the FMA pipe, the
+        // rest on the special-function unit; masked tiles use the latter only (exact zeros).
+        const bool split_exp = lim >= 63;
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          const float e0 = ex2_approx(fmaf(s[c], sl2, -mb));
-          const float e1 = ex2_approx(fmaf(s[c + 1], sl2, -mb));
+        for (int c = 0; c < 64; c += 2) {
+          const float x0 = fmaf(s[c], sl2, -mb), x1 = fmaf(s[c + 1], sl2, -mb);
+          float e0, e1;
+          if (((c >> 1) & 3) == 3 && split_exp) {
+            e0 = exp2_fma(x0);
+            e1 = exp2_fma(x1);
+          } else {
+            e0 = ex2_approx(x0);
+            e1 = ex2_approx(x1);
+          }
           sp[(c / 2) & 7] += e0 + e1;
           pk[c / 2] = Elem<T>::pack(e0, e1);
         }
         const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         l = l * alpha + rs;
-        // P row over columns 64-127 of this row's S (keys 2c, 2c+1 in column 64 + c)
-#pragma unroll
-        for (int c = 0; c < kBN / 64; ++c) {
-          tmem_st32(tS + 64 + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + c * 32));
-        }
-        // O_x *= alpha (after the S row is dead, to keep registers low): PV_x(t-1) has completed
-        // (S_x(t) was issued after it) and PV_x(t) waits for p_full below
+        // P over this group's 32 columns of the first half of S buffer b (after the exchange,
+        // so the other group has read its S columns there)
+        tmem_st32(tS + grp * 32, pk);
+        // O half-row *= alpha: O must hold PV(t-1) first, so wait for it (only when rescaling)
         if (__any_sync(0xffffffffu, resc)) {
+          if (t > 0 && !mbar_wait(pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const float a = resc ? alpha : 1.f;
           uint32_t r[32];
 #pragma unroll
-          for (int c = 0; c < DP / 32; ++c) {
+          for (int c = 0; c < DP / 64; ++c) {
             tmem_ld32(tO + c * 32, r);
             tmem_ld_wait();
             tmem_reg_fence(r);
@@ -438,15 +453,19 @@ __global__ void __launch_bounds__(384, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full + x);
+        mbar_arrive(p_full + b);
       }
       if (!ok) break;
       kv += it.n_kv;
-      // ---- epilogue: O / l and LSE, then release O_x for the next item's first PV
-      if (!mbar_wait(pv_done + x, (kv - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      // ---- epilogue: combine the two partial row sums, O / l and LSE
+      float lo;
+      if (!exchange(l, lo)) { ok = false; break; }
+      const float l_all = l + lo;
+      const uint32_t tl_last = kv - 1;
+      if (!mbar_wait(pv_done + (tl_last & 1), (tl_last >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const bool valid = q_row < it.seq_len;
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
       size_t row_off;
       if constexpr (VARLEN)
         row_off = (static_cast<size_t>(it.seq_start + q_row) * p.Hq + it.h) * p.d;
@@ -454,11 +473,11 @@ __global__ void __launch_bounds__(384, 1)
         row_off = ((static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row) * p.d;
       uint32_t r[32];
 #pragma unroll
-      for (int c = 0; c < DP / 32; ++c) {
+      for (int c = 0; c < DP / 64; ++c) {
         tmem_ld32(tO + c * 32, r);
         tmem_ld_wait();
         tmem_reg_fence(r);
-        const int col0 = c * 32;
+        const int col0 = grp * (DP / 2) + c * 32;
         if (valid && col0 < p.d) {
           const int ncol = min(32, p.d - col0);  // 16 or 32 (d is a multiple of 16)
           if (p.out_f32) {
@@ -486,9 +505,9 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(o_free + x);
-      if (valid && p.lse) {
-        const float lse = (m + __log2f(l)) * 0.69314718055994531f;
+      mbar_arrive(o_free);
+      if (grp == 0 && valid && p.lse) {
+        const float lse = (m + __log2f(l_all)) * 0.69314718055994531f;
         if constexpr (VARLEN)
           p.lse[static_cast<size_t>(it.h) * p.total_tokens + it.seq_start + q_row] = lse;
         else
@@ -518,19 +537,11 @@ inline int sm_count() {
 }
 
 template <typename T, int DP, bool CAUSAL, bool VARLEN>
-cudaError_t launch_fwd_tc_t(const FwdMaps& maps, const FwdParams& p_in, cudaStream_t stream) {
+cudaError_t launch_fwd_tc_t(const FwdMaps& maps, const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<DP>;
   auto kern = fwd_tc_kernel<T, DP, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  // The in-kernel register split assumes the launch allocation; never launch otherwise (an
-  // increase beyond what the block holds would wait forever).
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kern);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != static_cast<int>(L::kLaunchRegs)) return cudaErrorInvalidConfiguration;
-  FwdParams p = p_in;
-  p.n_qtiles = (p_in.n_qtiles + 1) / 2;  // pairs of query tiles
   const long heads = VARLEN ? static_cast<long>(p.Hq) * p.nseq : static_cast<long>(p.B) * p.Hq;
   const long items = heads * p.n_qtiles;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;

@@ -65,6 +65,19 @@ __device__ __forceinline__ void abort_set(uint32_t flag, int v) {
   asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(flag), "r"(v) : "memory");
 }
 
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  Returns false (after raising the abort
 // flag and, on a timeout, the device status) when the CTA must stop.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t abort_flag, unsigned* status) {
@@ -266,6 +279,23 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x on the FMA/ALU pipes, to take part of the exponentials off the special-function unit.
+// Range reduction in the manner of Cody and Waite: x = n + f with n = round(x), f in [-1/2, 1/2]
+// (adding 1.5 * 2^23 leaves round(x) in the low mantissa bits); 2^f from a degree-3 polynomial
+// whose coefficients were fitted for this library by the Remez exchange algorithm (minimax
+// relative error 7.5e-5 on [-1/2, 1/2]); 2^n added into the exponent field.  x is clamped to
+// -126 so the result stays normal: inputs below that give 2^-126 instead of (almost) 0.
+__device__ __forceinline__ float exp2_fma(float x) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  constexpr float c0 = 0.99992806f, c1 = 0.69326097f, c2 = 0.24261113f, c3 = 0.05517167f;
+  x = fmaxf(x, -126.0f);
+  const float t = x + kRound;
+  const float n = t - kRound;
+  const float f = x - n;
+  const float p = fmaf(fmaf(fmaf(c3, f, c2), f, c1), f, c0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
 }  // namespace attn
