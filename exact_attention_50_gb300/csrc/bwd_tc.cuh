@@ -123,8 +123,11 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kt = blockIdx.x;  // key tile; 0 first = the heaviest under the causal mask
-  const int b = blockIdx.y / p.Hkv, g = blockIdx.y % p.Hkv;
+  // Blocks are dispatched in linear order (x fastest): every (batch, kv head) of key tile 0,
+  // the heaviest under the causal mask, then key tile 1, ...; each SM that frees up takes the
+  // heaviest tile left, which keeps the causal tail short.
+  const int kt = blockIdx.y;
+  const int b = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
   const int N = p.N;
   const int n_q = (N + kBM - 1) / kBM;
   const int qt0 = CAUSAL ? kt : 0;
@@ -487,7 +490,7 @@ cudaError_t launch_bwd_tc_t(const BwdMaps& maps, const BwdParams& p, cudaStream_
   e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != static_cast<int>(L::kLaunchRegs)) return cudaErrorInvalidConfiguration;
-  const dim3 grid(p.n_ktiles, p.B * p.Hkv);
+  const dim3 grid(p.B * p.Hkv, p.n_ktiles);
   kern<<<grid, L::kThreads, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, maps.dout, p);
   return cudaGetLastError();
 }
