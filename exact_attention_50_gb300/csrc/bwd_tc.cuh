@@ -144,14 +144,14 @@ __global__ void __launch_bounds__(512, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, kEw);
+    mbar_init(p_full, kEw / 32);  // one arrival per warp
     mbar_init(dv_done, 1);
-    mbar_init(ds_full, kEw);
+    mbar_init(ds_full, kEw / 32);
     mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dq_free, 4);
     mbar_init(dkdv_done, 1);
-    mbar_init(rows_ready, kEw);
+    mbar_init(rows_ready, kEw / 32);
     mbar_init(drain, 1);
     abort_set(abort_flag, 0);
     mbar_init_fence();
@@ -227,52 +227,69 @@ __global__ void __launch_bounds__(512, 1)
         if (!mbar_wait(q_full + st, ph, abort_flag, p.status)) { ok = false; break; }
         if (it >= 1 && !mbar_wait(dv_done, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < DP / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + L::kColS, dK_k + off, dQ_k + st * kStage16 + off, idSS, ks > 0 ? 1u : 0u);
+        {
+          const uint64_t a = opaque(dK_k), bq = opaque(dQ_k + st * kStage16);
+#pragma unroll
+          for (int ks = 0; ks < DP / 16; ++ks) {
+            const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+            mma_ss(tmem + L::kColS, a + off, bq + off, idSS, ks > 0 ? 1u : 0u);
+          }
         }
         mma_commit(s_full);
         // ---- dP^T = V dO^T (needs dO and the dP columns: dQ of the previous tile read out)
         if (!mbar_wait(do_full + st, ph, abort_flag, p.status)) { ok = false; break; }
         if (it >= 1 && !mbar_wait(dq_free, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < DP / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + L::kColdP, dV_k + off, ddO_k + st * kStage16 + off, idSS, ks > 0 ? 1u : 0u);
+        {
+          const uint64_t a = opaque(dV_k), bo = opaque(ddO_k + st * kStage16);
+#pragma unroll
+          for (int ks = 0; ks < DP / 16; ++ks) {
+            const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+            mma_ss(tmem + L::kColdP, a + off, bo + off, idSS, ks > 0 ? 1u : 0u);
+          }
         }
         mma_commit(dp_full);
         // ---- dV += P^T dO; P^T hi/lo in TMEM: the 16 queries of k-step ks sit in the 32-column
         // group ks/2 (hi in its first 16 columns, lo in the last 16), 8 columns per k-step
         if (!mbar_wait(p_full, it & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint32_t acol = L::kColS + (ks >> 1) * 32 + (ks & 1) * 8;
-          const uint64_t bd = ddO_mn + st * kStage16 + ((ks * 2048) >> 4);
-          mma_ts(tmem + L::kColdV, tmem + acol, bd, idKD, (it > 0 || ks > 0) ? 1u : 0u);
-          mma_ts(tmem + L::kColdV, tmem + acol + 16, bd, idKD, 1u);
+        {
+          const uint64_t bo = opaque(ddO_mn + st * kStage16);
+          const uint32_t acc0 = it > 0 ? 1u : 0u;
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            const uint32_t acol = L::kColS + (ks >> 1) * 32 + (ks & 1) * 8;
+            const uint64_t bd = bo + ((ks * 2048) >> 4);
+            mma_ts(tmem + L::kColdV, tmem + acol, bd, idKD, ks > 0 ? 1u : acc0);
+            mma_ts(tmem + L::kColdV, tmem + acol + 16, bd, idKD, 1u);
+          }
         }
         mma_commit(dv_done);
         mma_commit(do_empty + st);
         // ---- dK += dS^T Q (hi, lo)
         if (!mbar_wait(ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint32_t a_off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-          const uint64_t bd = dQ_mn + st * kStage16 + ((ks * 2048) >> 4);
-          mma_ss(tmem + L::kColdK, dSh_k + a_off, bd, idKD, (it > 0 || ks > 0) ? 1u : 0u);
-          mma_ss(tmem + L::kColdK, dSl_k + a_off, bd, idKD, 1u);
+        {
+          const uint64_t ah = opaque(dSh_k), al = opaque(dSl_k), bq = opaque(dQ_mn + st * kStage16);
+          const uint32_t acc0 = it > 0 ? 1u : 0u;
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            const uint32_t a_off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+            const uint64_t bd = bq + ((ks * 2048) >> 4);
+            mma_ss(tmem + L::kColdK, ah + a_off, bd, idKD, ks > 0 ? 1u : acc0);
+            mma_ss(tmem + L::kColdK, al + a_off, bd, idKD, 1u);
+          }
         }
         mma_commit(q_empty + st);
         // ---- dQ_t = dS K (hi, lo), dS read MN-major from the dS^T tiles, into the dP columns
-#pragma unroll 1
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint32_t off = (ks * 2048) >> 4;
-          mma_ss(tmem + L::kColdQ, dSh_mn + off, dK_mn + off, idQ, ks > 0 ? 1u : 0u);
-          mma_ss(tmem + L::kColdQ, dSl_mn + off, dK_mn + off, idQ, 1u);
+        {
+          const uint64_t ah = opaque(dSh_mn), al = opaque(dSl_mn), bk = opaque(dK_mn);
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            const uint32_t off = (ks * 2048) >> 4;
+            mma_ss(tmem + L::kColdQ, ah + off, bk + off, idQ, ks > 0 ? 1u : 0u);
+            mma_ss(tmem + L::kColdQ, al + off, bk + off, idQ, 1u);
+          }
         }
         mma_commit(dq_full);
         mma_commit(ds_free);
@@ -295,7 +312,7 @@ __global__ void __launch_bounds__(512, 1)
     for (int it = 0; it < n_it; ++it) {
       const int h = g * p.G + it / per_head, qt = qt0 + it % per_head;
       const size_t row_base = (static_cast<size_t>(b) * p.Hq + h) * N;
-      if (!mbar_wait(dq_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!mbar_wait_warp(dq_full, it & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const int q = qt * kBM + t;
       float* dst = p.dq_acc + (row_base + q) * static_cast<size_t>(p.d);
@@ -309,7 +326,7 @@ __global__ void __launch_bounds__(512, 1)
         tmem_reg_fence(r1);
         if (c2 == DP / 64 - 1) {
           tc_fence_before();
-          mbar_arrive(dq_free);  // the dQ columns may be overwritten once everything is loaded
+          mbar_arrive_warp(dq_free);  // the dQ columns may be overwritten once everything is loaded
         }
         if (q < N) {
 #pragma unroll
@@ -330,7 +347,7 @@ __global__ void __launch_bounds__(512, 1)
       }
     }
     // ---- epilogue: dK (scaled) and dV rows of this key tile
-    if (ok && mbar_wait(dkdv_done, 0, abort_flag, p.status)) {
+    if (ok && mbar_wait_warp(dkdv_done, 0, abort_flag, p.status)) {
       tc_fence_after();
       const int key = kt * kBN + t;
       const size_t krow = (static_cast<size_t>(b) * p.Hkv + g) * N + key;
@@ -401,10 +418,10 @@ __global__ void __launch_bounds__(512, 1)
         lse_buf[threadIdx.x] = lse_next;
         d_buf[threadIdx.x] = d_next;
       }
-      mbar_arrive(rows_ready);
-      if (!mbar_wait(rows_ready, it & 1, abort_flag, p.status)) break;
+      mbar_arrive_warp(rows_ready);
+      if (!mbar_wait_warp(rows_ready, it & 1, abort_flag, p.status)) break;
       // ---- phase 1: P^T = exp2(S^T * scale * log2e - LSE * log2e), hi/lo back into TMEM
-      if (!mbar_wait(s_full, it & 1, abort_flag, p.status)) break;
+      if (!mbar_wait_warp(s_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
       float pv[64];
       {
@@ -434,11 +451,11 @@ __global__ void __launch_bounds__(512, 1)
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive_warp(p_full);
       load_rows(it + 1);  // prefetch the next tile's LSE and D
       // ---- phase 2: dS^T = P^T (dP^T - D), hi/lo into shared memory
-      if (it >= 1 && !mbar_wait(ds_free, (it - 1) & 1, abort_flag, p.status)) break;
-      if (!mbar_wait(dp_full, it & 1, abort_flag, p.status)) break;
+      if (it >= 1 && !mbar_wait_warp(ds_free, (it - 1) & 1, abort_flag, p.status)) break;
+      if (!mbar_wait_warp(dp_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
       {
         uint32_t r0[32], r1[32];
@@ -467,7 +484,7 @@ __global__ void __launch_bounds__(512, 1)
         *reinterpret_cast<uint4*>(sdSl + off) = c;
       }
       fence_async_smem();
-      mbar_arrive(ds_full);
+      mbar_arrive_warp(ds_full);
     }
   }
 

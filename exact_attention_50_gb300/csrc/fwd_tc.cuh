@@ -15,13 +15,15 @@
 //              Thread t of either group owns query row t (TMEM lane t).  The two threads of a
 //              row exchange their partial row maxima through shared memory, so both use the
 //              same running max; each keeps its own partial row sum, combined at the end.  Each
-//              writes its 64 P values (16-bit) back over the first half of the S tile's columns,
+//              writes its 64 P values (16-bit pairs) into its 32 columns of the P buffer,
 //              rescales its half of the O row when the max moved, and writes that half of O.
 //   warp 8     TMA producer (lane 0) and TMEM allocator (whole warp).
 //   warp 9     MMA issuer (lane 0): a non-blocking scheduler over the streams S(j) and PV(j).
-// TMEM: S double buffer at columns [0,128) and [128,256), O at [256, 256+DP).  S(j) goes into
-// buffer j % 2, where P(j-2) lives, so it waits only for PV(j-2) -- long finished -- and the
-// tensor core computes S(j+1) while the softmax works on S(j).
+// TMEM: S double buffer at columns [0,128) and [128,256), P double buffer (16-bit pairs) at
+// [256,320) and [320,384), O at [384, 384+DP).  S(j) goes into S buffer j % 2 as soon as the
+// softmax has loaded S(j-2) into registers, and P(j) into P buffer j % 2 once PV(j-2) has read
+// P(j-2): no MMA waits for another MMA, and the tensor core computes S(j+1) (and S(j+2)) while
+// the softmax works on S(j).
 //
 // Lazy rescaling: the running max used for the exponentials is only moved when a tile's max
 // exceeds it by more than kRescaleLog2 (log2 units); the final O / l and LSE use the same max,
@@ -65,13 +67,14 @@ struct FwdLayout {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffX = kOffV + kStages * kTileBytes;  // exchange [2 slots][2 groups][128 rows]
   static constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
-  // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-  // pv_done[2], o_free, xch[2], drain
-  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 1 + 2 + 1;
+  // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], s_free[2],
+  // p_full[2], pv_done[2], o_free, xch[2], drain
+  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 2 + 1 + 2 + 1;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base (u32), abort flag (int)
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;         // slack for 1024-byte alignment
   static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColP = 256, kColO = 384;
   static constexpr int kThreads = 320;
 };
 
@@ -141,10 +144,11 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* k_empty = k_full + S;
   uint64_t* v_full = k_empty + S;
   uint64_t* v_empty = v_full + S;
-  // Per S buffer b: s_full (S(j) ready), p_full (P(j) written over it), pv_done (PV(j) done),
-  // for the tiles j with j % 2 == b; phase k of each is tile 2k + b.
+  // Per buffer b: s_full (S(j) ready), s_free (S(j) loaded by the softmax), p_full (P(j)
+  // written), pv_done (PV(j) done), for the tiles j with j % 2 == b; phase k is tile 2k + b.
   uint64_t* s_full = v_empty + S;
-  uint64_t* p_full = s_full + 2;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_free = pv_done + 2;
   uint64_t* xch = o_free + 1;       // [2]: row-max / row-sum exchange slots
@@ -165,11 +169,12 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 256);
+      mbar_init(s_free + i, 8);  // one arrival per softmax warp
+      mbar_init(p_full + i, 8);
       mbar_init(pv_done + i, 1);
-      mbar_init(xch + i, 256);
+      mbar_init(xch + i, 8);
     }
-    mbar_init(o_free, 256);
+    mbar_init(o_free, 8);
     mbar_init(drain, 1);
     abort_set(abort_flag, 0);
     mbar_init_fence();
@@ -253,29 +258,34 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
       uint32_t ic = 0;
       bool ok = true;
+      // Each group is a straight run of MMAs: one base per operand, compile-time offsets, no
+      // branch between two MMAs (a branch or per-MMA address arithmetic there halves the rate
+      // at which one thread can feed the tensor core).
       auto issue_s = [&](uint32_t t) {
         const uint64_t kx = dK + (((t % S) * L::kTileBytes) >> 4);
+        const uint32_t d = tmem + (t & 1) * 128;
         tc_fence_after();
-#pragma unroll 1
+#pragma unroll
         for (int ks = 0; ks < DP / 16; ++ks) {
           const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + (t & 1) * 128, dQ + off, kx + off, idS, ks > 0 ? 1u : 0u);
+          mma_ss(d, dQ + off, kx + off, idS, ks > 0 ? 1u : 0u);
         }
         mma_commit(s_full + (t & 1));
       };
       auto issue_pv = [&](uint32_t t, bool first) {
         tc_fence_after();
         const uint64_t vx = dV + (((t % S) * L::kTileBytes) >> 4);
-        // P(t) over columns [0,64) of S buffer t % 2: keys 2c, 2c+1 in column c
-#pragma unroll 1
+        // P(t) in P buffer t % 2: keys 2c, 2c+1 in column c
+        const uint32_t pa = tmem + L::kColP + (t & 1) * 64;
+        const uint32_t acc0 = first ? 0u : 1u;
+#pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_ts(tmem + 256, tmem + (t & 1) * 128 + ks * 8, vx + ((ks * 2048) >> 4), idO,
-                 (!first || ks > 0) ? 1u : 0u);
+          mma_ts(tmem + L::kColO, pa + ks * 8, vx + ((ks * 2048) >> 4), idO, ks > 0 ? 1u : acc0);
         mma_commit(pv_done + (t & 1));
         mma_commit(v_empty + t % S);
       };
       // A small scheduler over the two streams, polled without blocking:
-      //   S(j)  needs Q, K_j, and PV(j-2) complete (S(j) overwrites P(j-2) in buffer j % 2);
+      //   S(j)  needs Q, K_j, and S(j-2) loaded by the softmax (S buffer j % 2 free);
       //   PV(j) needs P(j) (p_full) and V_j, and for an item's first tile the previous item's O
       //         read out (o_free).
       // K_j is released once S(j) is issued, Q once the item's last S is.  Every barrier tested
@@ -293,8 +303,8 @@ __global__ void __launch_bounds__(320, 1)
           bool progress = false;
           if (!q_ready) q_ready = mbar_test(q_full, ic & 1);
           const uint32_t ts = t0 + ns;
-          if (q_ready && ns < n && ns <= np + 1 && mbar_test(k_full + ts % S, (ts / S) & 1) &&
-              (ts < 2 || mbar_test(pv_done + (ts & 1), ((ts - 2) >> 1) & 1))) {
+          if (q_ready && ns < n && mbar_test(k_full + ts % S, (ts / S) & 1) &&
+              (ts < 2 || mbar_test(s_free + (ts & 1), ((ts - 2) >> 1) & 1))) {
             issue_s(ts);
             mma_commit(k_empty + ts % S);
             ++ns;
@@ -337,7 +347,7 @@ __global__ void __launch_bounds__(320, 1)
     const int grp = warp >> 2;                // 0: key columns 0-63, 1: key columns 64-127
     const int row = threadIdx.x & 127;        // TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t tO = tl + 256 + grp * (DP / 2);  // this group's half of the O row
+    const uint32_t tO = tl + L::kColO + grp * (DP / 2);  // this group's half of the O row
     const float sl2 = p.scale_log2;
     uint32_t kv = 0, ic = 0;
     uint32_t xc = 0;  // exchanges done (slot xc % 2, phase (xc / 2) % 2)
@@ -346,10 +356,8 @@ __global__ void __launch_bounds__(320, 1)
     auto exchange = [&](float v, float& other) -> bool {
       float* xb = sX + (xc & 1) * 256;
       xb[grp * 128 + row] = v;
-      tc_fence_before();  // also orders this thread's S reads before the other group's P writes
-      mbar_arrive(xch + (xc & 1));
-      if (!mbar_wait(xch + (xc & 1), (xc >> 1) & 1, abort_flag, p.status)) return false;
-      tc_fence_after();
+      mbar_arrive_warp(xch + (xc & 1));
+      if (!mbar_wait_warp(xch + (xc & 1), (xc >> 1) & 1, abort_flag, p.status)) return false;
       other = xb[(grp ^ 1) * 128 + row];
       ++xc;
       return true;
@@ -362,7 +370,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t t = kv + j;
         const int b = t & 1;
-        if (!mbar_wait(s_full + b, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!mbar_wait_warp(s_full + b, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tS = tl + b * 128;
         float s[64];
@@ -379,6 +387,8 @@ __global__ void __launch_bounds__(320, 1)
             s[32 + i] = __uint_as_float(r1[i]);
           }
         }
+        tc_fence_before();
+        mbar_arrive_warp(s_free + b);  // S buffer b may take S(t+2)
         // keys key0 + c with c > lim are masked (past the diagonal, or past the sequence)
         const int key0 = j * kBN + grp * 64;
         const int lim = CAUSAL ? min(q_row, it.seq_len - 1) - key0 : it.seq_len - 1 - key0;
@@ -429,12 +439,13 @@ __global__ void __launch_bounds__(320, 1)
         }
         const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         l = l * alpha + rs;
-        // P over this group's 32 columns of the first half of S buffer b (after the exchange,
-        // so the other group has read its S columns there)
-        tmem_st32(tS + grp * 32, pk);
+        // P over this group's 32 columns of P buffer b, free once PV(t-2) has read P(t-2)
+        if (t >= 2 && !mbar_wait_warp(pv_done + b, ((t >> 1) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        tmem_st32(tl + L::kColP + b * 64 + grp * 32, pk);
         // O half-row *= alpha: O must hold PV(t-1) first, so wait for it (only when rescaling)
         if (__any_sync(0xffffffffu, resc)) {
-          if (t > 0 && !mbar_wait(pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, p.status)) {
+          if (t > 0 && !mbar_wait_warp(pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -453,7 +464,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full + b);
+        mbar_arrive_warp(p_full + b);
       }
       if (!ok) break;
       kv += it.n_kv;
@@ -462,7 +473,7 @@ __global__ void __launch_bounds__(320, 1)
       if (!exchange(l, lo)) { ok = false; break; }
       const float l_all = l + lo;
       const uint32_t tl_last = kv - 1;
-      if (!mbar_wait(pv_done + (tl_last & 1), (tl_last >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!mbar_wait_warp(pv_done + (tl_last & 1), (tl_last >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const bool valid = q_row < it.seq_len;
       const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
@@ -505,7 +516,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(o_free);
+      mbar_arrive_warp(o_free);
       if (grp == 0 && valid && p.lse) {
         const float lse = (m + __log2f(l_all)) * 0.69314718055994531f;
         if constexpr (VARLEN)

@@ -97,6 +97,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
+// Bounded wait taken by a whole warp: every lane gets the same answer (false if any lane's
+// wait failed), so the warp leaves a loop together and later warp-wide operations stay safe.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t abort_flag,
+                                               unsigned* status) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// One arrival for the whole warp (the barrier counts warps, not threads).  Arrivals on one
+// mbarrier are atomic updates of one shared-memory word and serialise, so a warp arrives once:
+// the __syncwarp orders every lane's earlier work (after the caller's fences) before lane 0's
+// release-arrive.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // A short bounded wait used only on the abort path, to let copies already in flight land
 // before the CTA exits.  Never raises a status.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
@@ -254,6 +271,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool a_mn_major, boo
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((static_cast<uint32_t>(N) >> 3) << 17) |
          ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+
+// Hides a value from the optimiser at this point: expressions derived from it are computed
+// here instead of being hoisted out of the enclosing loop and kept live in registers.
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  asm volatile("" : "+l"(x));
+  return x;
 }
 
 // ------------------------------------------------------------------ register split
