@@ -59,20 +59,25 @@ constexpr float kRescaleLog2 = 8.0f;
 
 template <int DP>
 struct FwdLayout {
-  static constexpr int kStages = DP == 128 ? 2 : 4;
+  // For d = 128 one Q tile and three K and three V tiles in flight (224 KB in all): an L2
+  // load takes up to ~3000 cycles when every SM streams K and V, about two tiles of work.
+  // d = 64 double-buffers Q as well (the next item's Q loads while the current one is used).
+  static constexpr int kStagesQ = DP == 128 ? 1 : 2;
+  static constexpr int kStagesK = DP == 128 ? 3 : 4;
+  static constexpr int kStagesV = DP == 128 ? 3 : 4;
   static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 64 elements x 2 B
   static constexpr int kTileBytes = (DP / 64) * kChunkBytes;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffX = kOffV + kStages * kTileBytes;  // exchange [2 slots][2 groups][128 rows]
+  static constexpr int kOffK = kOffQ + kStagesQ * kTileBytes;
+  static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
+  static constexpr int kOffX = kOffV + kStagesV * kTileBytes;  // exchange [2 slots][2 groups][128 rows]
   static constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
-  // q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], s_free[2],
-  // p_full[2], pv_done[2], o_free, xch[2], drain
-  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 2 + 1 + 2 + 1;
+  // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
+  // s_free[2], p_full[2], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base (u32), abort flag (int)
   static constexpr int kBytes = kOffMisc + 16;
-  static constexpr int kSmemAlloc = kBytes + 1024;         // slack for 1024-byte alignment
+  static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColP = 256, kColO = 384;
   static constexpr int kThreads = 320;
@@ -124,46 +129,90 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int idx) {
   return it;
 }
 
+// Walks the key tiles of a CTA's work items in order (item by item, key tile by key tile).
+// The producer and the MMA issuer each run such walks for their streams (Q/K, V; S, PV).
+template <bool CAUSAL, bool VARLEN>
+struct TileCursor {
+  int idx, j;   // work item index and key tile within it
+  uint32_t t;   // key tiles passed so far: ring position and barrier phases, across items
+  uint32_t ic;  // items passed so far
+  FwdItem it;
+  bool done;
+  __device__ __forceinline__ void seek(const FwdParams& p, int n_items) {
+    for (; idx < n_items; idx += gridDim.x) {
+      it = fwd_item<CAUSAL, VARLEN>(p, idx);
+      if (it.valid) return;
+    }
+    done = true;
+  }
+  __device__ __forceinline__ void start(const FwdParams& p, int n_items) {
+    idx = blockIdx.x;
+    j = 0;
+    t = 0;
+    ic = 0;
+    done = false;
+    seek(p, n_items);
+  }
+  __device__ __forceinline__ void advance(const FwdParams& p, int n_items) {
+    ++t;
+    if (++j < it.n_kv) return;
+    j = 0;
+    ++ic;
+    idx += gridDim.x;
+    seek(p, n_items);
+  }
+};
+
 template <typename T, int DP, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(320, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p, int n_items) {
   using L = FwdLayout<DP>;
-  constexpr int S = L::kStages;
+  constexpr int SQ = L::kStagesQ, SK = L::kStagesK, SV = L::kStagesV;
   constexpr int kChunks = DP / 64;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The 128-byte swizzle atoms need 1024-byte aligned tiles and the layout has no slack to
+  // realign: refuse to run (before any barrier or allocation) if the base is not aligned.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) raise_status(p.status, ATTN_ERR_CUDA);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sQ = smem + L::kOffQ;
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
   float* sX = reinterpret_cast<float*>(smem + L::kOffX);  // [slot][group][row]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-  uint64_t* q_full = bars;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* k_empty = k_full + S;
-  uint64_t* v_full = k_empty + S;
-  uint64_t* v_empty = v_full + S;
+  uint64_t* q_full = bars;       // [2]: item i uses Q slot i % SQ
+  uint64_t* q_empty = bars + 2;  // [2]
+  uint64_t* k_full = bars + 4;
+  uint64_t* k_empty = k_full + SK;
+  uint64_t* v_full = k_empty + SK;
+  uint64_t* v_empty = v_full + SV;
   // Per buffer b: s_full (S(j) ready), s_free (S(j) loaded by the softmax), p_full (P(j)
   // written), pv_done (PV(j) done), for the tiles j with j % 2 == b; phase k is tile 2k + b.
-  uint64_t* s_full = v_empty + S;
+  uint64_t* s_full = v_empty + SV;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* o_free = pv_done + 2;
-  uint64_t* xch = o_free + 1;       // [2]: row-max / row-sum exchange slots
-  uint64_t* drain = xch + 2;
+  uint64_t* xch = o_free + 1;       // [quadrant][slot]: row-max / row-sum exchange, warps q and q + 4
+  uint64_t* drain = xch + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int i = 0; i < S; ++i) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full + i, 1);
+      mbar_init(q_empty + i, 1);
+    }
+    for (int i = 0; i < SK; ++i) {
       mbar_init(k_full + i, 1);
       mbar_init(k_empty + i, 1);
+    }
+    for (int i = 0; i < SV; ++i) {
       mbar_init(v_full + i, 1);
       mbar_init(v_empty + i, 1);
     }
@@ -172,9 +221,9 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(s_free + i, 8);  // one arrival per softmax warp
       mbar_init(p_full + i, 8);
       mbar_init(pv_done + i, 1);
-      mbar_init(xch + i, 8);
     }
     mbar_init(o_free, 8);
+    for (int i = 0; i < 8; ++i) mbar_init(xch + i, 2);  // the two warps of a row quadrant
     mbar_init(drain, 1);
     abort_set(abort_flag, 0);
     mbar_init_fence();
@@ -187,60 +236,93 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ================================================================ TMA producer
+    // Two streams over the same sequence of key tiles, polled without blocking: K (with each
+    // item's Q) and V.  Neither waits behind the other, so K tiles run ahead into their
+    // deeper ring while V waits for its PV to free a slot.  Every barrier tested here cannot
+    // complete its next phase before this thread issues another copy, so no phase is skipped.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t kv = 0;  // key tiles issued so far (ring position), across items
-      uint32_t ic = 0;  // items processed
-      uint32_t nk_issued = 0, nv_issued = 0;
+      TileCursor<CAUSAL, VARLEN> ck, cv;
+      ck.start(p, n_items);
+      cv.start(p, n_items);
+      uint32_t nq = 0;      // Q tiles issued (one per item, slot item % 2)
+      bool q_cur = false;   // the Q of ck's item has been issued
       bool ok = true;
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
-        const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
-        if (!it.valid) continue;
-        if (ic > 0 && !mbar_wait(q_empty, (ic - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        mbar_expect_tx(q_full, L::kTileBytes);
-        for (int c = 0; c < kChunks; ++c) {
-          uint8_t* dst = sQ + c * L::kChunkBytes;
-          if constexpr (VARLEN)
-            tma_load_4d(dst, &tmQ, q_full, c * 64, it.h, 0, it.seq_start + it.qt * kBM);
-          else
-            tma_load_3d(dst, &tmQ, q_full, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
-        }
-        const int g = it.h / p.G;
-        for (int j = 0; j < it.n_kv; ++j, ++kv) {
-          const int st = kv % S;
-          const uint32_t ph = ((kv / S) - 1) & 1;
-          if (kv >= S && !mbar_wait(k_empty + st, ph, abort_flag, p.status)) { ok = false; break; }
-          mbar_expect_tx(k_full + st, L::kTileBytes);
+      unsigned long long t_idle = 0;
+      while (!ck.done || !cv.done) {
+        bool progress = false;
+        const uint32_t qs = nq % SQ;
+        if (!ck.done && !q_cur && (nq < static_cast<uint32_t>(SQ) || mbar_test(q_empty + qs, ((nq / SQ) - 1) & 1))) {
+          const FwdItem& it = ck.it;
+          mbar_expect_tx(q_full + qs, L::kTileBytes);
           for (int c = 0; c < kChunks; ++c) {
-            uint8_t* dst = sK + st * L::kTileBytes + c * L::kChunkBytes;
+            uint8_t* dst = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
             if constexpr (VARLEN)
-              tma_load_4d(dst, &tmK, k_full + st, c * 64, it.h, 1, it.seq_start + j * kBN);
+              tma_load_4d(dst, &tmQ, q_full + qs, c * 64, it.h, 0, it.seq_start + it.qt * kBM);
             else
-              tma_load_3d(dst, &tmK, k_full + st, c * 64, j * kBN, it.b * p.Hkv + g);
+              tma_load_3d(dst, &tmQ, q_full + qs, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
           }
-          nk_issued = kv + 1;
-          if (kv >= S && !mbar_wait(v_empty + st, ph, abort_flag, p.status)) { ok = false; break; }
-          mbar_expect_tx(v_full + st, L::kTileBytes);
-          for (int c = 0; c < kChunks; ++c) {
-            uint8_t* dst = sV + st * L::kTileBytes + c * L::kChunkBytes;
-            if constexpr (VARLEN)
-              tma_load_4d(dst, &tmV, v_full + st, c * 64, it.h, 2, it.seq_start + j * kBN);
-            else
-              tma_load_3d(dst, &tmV, v_full + st, c * 64, j * kBN, it.b * p.Hkv + g);
-          }
-          nv_issued = kv + 1;
+          ++nq;
+          q_cur = true;
+          progress = true;
         }
-        ++ic;
+        if (!ck.done && q_cur) {
+          const uint32_t st = ck.t % SK;
+          if (ck.t < static_cast<uint32_t>(SK) || mbar_test(k_empty + st, ((ck.t / SK) - 1) & 1)) {
+            const FwdItem& it = ck.it;
+            mbar_expect_tx(k_full + st, L::kTileBytes);
+            for (int c = 0; c < kChunks; ++c) {
+              uint8_t* dst = sK + st * L::kTileBytes + c * L::kChunkBytes;
+              if constexpr (VARLEN)
+                tma_load_4d(dst, &tmK, k_full + st, c * 64, it.h, 1, it.seq_start + ck.j * kBN);
+              else
+                tma_load_3d(dst, &tmK, k_full + st, c * 64, ck.j * kBN, it.b * p.Hkv + it.h / p.G);
+            }
+            ck.advance(p, n_items);
+            if (ck.j == 0) q_cur = false;  // the next K belongs to a new item: its Q comes first
+            progress = true;
+          }
+        }
+        if (!cv.done) {
+          const uint32_t st = cv.t % SV;
+          if (cv.t < static_cast<uint32_t>(SV) || mbar_test(v_empty + st, ((cv.t / SV) - 1) & 1)) {
+            const FwdItem& it = cv.it;
+            mbar_expect_tx(v_full + st, L::kTileBytes);
+            for (int c = 0; c < kChunks; ++c) {
+              uint8_t* dst = sV + st * L::kTileBytes + c * L::kChunkBytes;
+              if constexpr (VARLEN)
+                tma_load_4d(dst, &tmV, v_full + st, c * 64, it.h, 2, it.seq_start + cv.j * kBN);
+              else
+                tma_load_3d(dst, &tmV, v_full + st, c * 64, cv.j * kBN, it.b * p.Hkv + it.h / p.G);
+            }
+            cv.advance(p, n_items);
+            progress = true;
+          }
+        }
+        if (progress) {
+          t_idle = 0;
+        } else {
+          const unsigned long long now = globaltimer();
+          if (t_idle == 0) t_idle = now;
+          if (abort_read(abort_flag)) { ok = false; break; }
+          if (now - t_idle > kWaitTimeoutNs) {
+            raise_status(p.status, ATTN_ERR_TIMEOUT);
+            abort_set(abort_flag, 1);
+            ok = false;
+            break;
+          }
+        }
       }
-      if (abort_read(abort_flag)) {
+      if (!ok || abort_read(abort_flag)) {
         // let the copies already issued land before the CTA's shared memory goes away
-        if (ic > 0) mbar_drain(q_full, (ic - 1) & 1);
-        for (uint32_t j = nk_issued > (uint32_t)S ? nk_issued - S : 0; j < nk_issued; ++j)
-          mbar_drain(k_full + j % S, (j / S) & 1);
-        for (uint32_t j = nv_issued > (uint32_t)S ? nv_issued - S : 0; j < nv_issued; ++j)
-          mbar_drain(v_full + j % S, (j / S) & 1);
+        for (uint32_t n = nq > static_cast<uint32_t>(SQ) ? nq - SQ : 0; n < nq; ++n)
+          mbar_drain(q_full + n % SQ, (n / SQ) & 1);
+        for (uint32_t j = ck.t > static_cast<uint32_t>(SK) ? ck.t - SK : 0; j < ck.t; ++j)
+          mbar_drain(k_full + j % SK, (j / SK) & 1);
+        for (uint32_t j = cv.t > static_cast<uint32_t>(SV) ? cv.t - SV : 0; j < cv.t; ++j)
+          mbar_drain(v_full + j % SV, (j / SV) & 1);
       }
     }
     __syncwarp();
@@ -255,26 +337,25 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV = smem_desc_sw128(smem_u32(sV), L::kChunkBytes, 1024);
-      uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
-      uint32_t ic = 0;
       bool ok = true;
       // Each group is a straight run of MMAs: one base per operand, compile-time offsets, no
       // branch between two MMAs (a branch or per-MMA address arithmetic there halves the rate
       // at which one thread can feed the tensor core).
-      auto issue_s = [&](uint32_t t) {
-        const uint64_t kx = dK + (((t % S) * L::kTileBytes) >> 4);
+      auto issue_s = [&](uint32_t t, uint32_t qs) {
+        const uint64_t qx = dQ + ((qs * L::kTileBytes) >> 4);
+        const uint64_t kx = dK + (((t % SK) * L::kTileBytes) >> 4);
         const uint32_t d = tmem + (t & 1) * 128;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < DP / 16; ++ks) {
           const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-          mma_ss(d, dQ + off, kx + off, idS, ks > 0 ? 1u : 0u);
+          mma_ss(d, qx + off, kx + off, idS, ks > 0 ? 1u : 0u);
         }
         mma_commit(s_full + (t & 1));
       };
       auto issue_pv = [&](uint32_t t, bool first) {
         tc_fence_after();
-        const uint64_t vx = dV + (((t % S) * L::kTileBytes) >> 4);
+        const uint64_t vx = dV + (((t % SV) * L::kTileBytes) >> 4);
         // P(t) in P buffer t % 2: keys 2c, 2c+1 in column c
         const uint32_t pa = tmem + L::kColP + (t & 1) * 64;
         const uint32_t acc0 = first ? 0u : 1u;
@@ -282,37 +363,41 @@ __global__ void __launch_bounds__(320, 1)
         for (int ks = 0; ks < kBN / 16; ++ks)
           mma_ts(tmem + L::kColO, pa + ks * 8, vx + ((ks * 2048) >> 4), idO, ks > 0 ? 1u : acc0);
         mma_commit(pv_done + (t & 1));
-        mma_commit(v_empty + t % S);
+        mma_commit(v_empty + t % SV);
       };
-      // A small scheduler over the two streams, polled without blocking:
+      // A small scheduler over the two streams of an item, polled without blocking:
       //   S(j)  needs Q, K_j, and S(j-2) loaded by the softmax (S buffer j % 2 free);
       //   PV(j) needs P(j) (p_full) and V_j, and for an item's first tile the previous item's O
       //         read out (o_free).
       // K_j is released once S(j) is issued, Q once the item's last S is.  Every barrier tested
       // here cannot complete its next phase before this thread issues something, so a phase is
-      // never skipped between two polls.
+      // never skipped between two polls.  (Letting S run on into the next item while the last
+      // PVs of this one are pending measured slower: those PVs gate the item's epilogue.)
+      uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
+      uint32_t ic = 0;
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
         const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
         if (!it.valid) continue;
         const int n = it.n_kv;
         const uint32_t t0 = kv;
+        const uint32_t qs = ic % SQ;
         int ns = 0, np = 0;
         bool q_ready = false;
         unsigned long long t_idle = 0;
         while (np < n) {
           bool progress = false;
-          if (!q_ready) q_ready = mbar_test(q_full, ic & 1);
+          if (!q_ready) q_ready = mbar_test(q_full + qs, (ic / SQ) & 1);
           const uint32_t ts = t0 + ns;
-          if (q_ready && ns < n && mbar_test(k_full + ts % S, (ts / S) & 1) &&
+          if (q_ready && ns < n && mbar_test(k_full + ts % SK, (ts / SK) & 1) &&
               (ts < 2 || mbar_test(s_free + (ts & 1), ((ts - 2) >> 1) & 1))) {
-            issue_s(ts);
-            mma_commit(k_empty + ts % S);
+            issue_s(ts, qs);
+            mma_commit(k_empty + ts % SK);
             ++ns;
-            if (ns == n) mma_commit(q_empty);
+            if (ns == n) mma_commit(q_empty + qs);
             progress = true;
           }
           const uint32_t tp = t0 + np;
-          if (np < ns && mbar_test(p_full + (tp & 1), (tp >> 1) & 1) && mbar_test(v_full + tp % S, (tp / S) & 1) &&
+          if (np < ns && mbar_test(p_full + (tp & 1), (tp >> 1) & 1) && mbar_test(v_full + tp % SV, (tp / SV) & 1) &&
               (np > 0 || ic == 0 || mbar_test(o_free, (ic - 1) & 1))) {
             issue_pv(tp, np == 0);
             ++np;
@@ -356,8 +441,9 @@ __global__ void __launch_bounds__(320, 1)
     auto exchange = [&](float v, float& other) -> bool {
       float* xb = sX + (xc & 1) * 256;
       xb[grp * 128 + row] = v;
-      mbar_arrive_warp(xch + (xc & 1));
-      if (!mbar_wait_warp(xch + (xc & 1), (xc >> 1) & 1, abort_flag, p.status)) return false;
+      uint64_t* bar = xch + (warp & 3) * 2 + (xc & 1);
+      mbar_arrive_warp(bar);
+      if (!mbar_wait_warp(bar, (xc >> 1) & 1, abort_flag, p.status)) return false;
       other = xb[(grp ^ 1) * 128 + row];
       ++xc;
       return true;
@@ -396,16 +482,19 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) s[c] = c > lim ? -INFINITY : s[c];
         }
-        // partial row max with 8 independent chains, then the other group's
-        float mp[8];
+        // partial row max (3-input max, 4 chains), then the other group's
+        float m0 = max3f(s[0], s[1], s[2]), m1 = max3f(s[3], s[4], s[5]);
+        float m2 = max3f(s[6], s[7], s[8]), m3 = max3f(s[9], s[10], s[11]);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mp[k] = s[k];
-#pragma unroll
-        for (int c = 8; c < 64; c += 8)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[c + k]);
-        float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                         fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        for (int c = 12; c < 60; c += 8) {
+          m0 = max3f(m0, s[c], s[c + 1]);
+          m1 = max3f(m1, s[c + 2], s[c + 3]);
+          m2 = max3f(m2, s[c + 4], s[c + 5]);
+          m3 = max3f(m3, s[c + 6], s[c + 7]);
+        }
+        m0 = max3f(m0, s[60], s[61]);
+        m1 = max3f(m1, s[62], s[63]);
+        float mx = max3f(m0, m1, fmaxf(m2, m3));
         float mo;
         if (!exchange(mx, mo)) { ok = false; break; }
         mx = fmaxf(mx, mo);
@@ -418,26 +507,40 @@ __global__ void __launch_bounds__(320, 1)
           m = mx2;
         }
         const float mb = (m == -INFINITY) ? 0.f : m;
-        float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 partial row sums
+        // exponentials in pairs: x = s * scale * log2(e) - m with one paired FMA, 2^x, the row
+        // sum in 4 paired chains, and the 16-bit pair of P.  In tiles with no masked key a
+        // quarter of the exponentials run on the FMA pipe, the rest on the special-function
+        // unit; masked tiles use the latter only (exact zeros).
+        const uint64_t scl = f2_pack(sl2, sl2), nmb = f2_pack(-mb, -mb);
+        uint64_t acc[4];
         uint32_t pk[32];
-        // In tiles with no masked key a quarter of the exponentials run on the FMA pipe, the
-        // rest on the special-function unit; masked tiles use the latter only (exact zeros).
-        const bool split_exp = lim >= 63;
+        if (lim >= 63) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float x0 = fmaf(s[c], sl2, -mb), x1 = fmaf(s[c + 1], sl2, -mb);
-          float e0, e1;
-          if (((c >> 1) & 3) == 3 && split_exp) {
-            e0 = exp2_fma(x0);
-            e1 = exp2_fma(x1);
-          } else {
-            e0 = ex2_approx(x0);
-            e1 = ex2_approx(x1);
+          for (int c = 0; c < 64; c += 2) {
+            const uint64_t x = f2_fma(f2_pack(s[c], s[c + 1]), scl, nmb);
+            uint64_t e;
+            if (((c >> 1) & 3) == 3) {
+              e = exp2_fma2(x);
+            } else {
+              const float2 xf = f2_unpack(x);
+              e = f2_pack(ex2_approx(xf.x), ex2_approx(xf.y));
+            }
+            acc[(c >> 1) & 3] = c < 8 ? e : f2_add(acc[(c >> 1) & 3], e);
+            const float2 ef = f2_unpack(e);
+            pk[c / 2] = Elem<T>::pack(ef.x, ef.y);
           }
-          sp[(c / 2) & 7] += e0 + e1;
-          pk[c / 2] = Elem<T>::pack(e0, e1);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float2 xf = f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), scl, nmb));
+            const float e0 = ex2_approx(xf.x), e1 = ex2_approx(xf.y);
+            const uint64_t e = f2_pack(e0, e1);
+            acc[(c >> 1) & 3] = c < 8 ? e : f2_add(acc[(c >> 1) & 3], e);
+            pk[c / 2] = Elem<T>::pack(e0, e1);
+          }
         }
-        const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        const float2 rs2 = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
+        const float rs = rs2.x + rs2.y;
         l = l * alpha + rs;
         // P over this group's 32 columns of P buffer b, free once PV(t-2) has read P(t-2)
         if (t >= 2 && !mbar_wait_warp(pv_done + b, ((t >> 1) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
