@@ -56,6 +56,11 @@ struct Elem<__half> {
 };
 
 constexpr float kRescaleLog2 = 8.0f;
+// Which of every 8 exponential pairs run on the FMA pipe (bit k: pair k) instead of the
+// special-function unit.  None: at 32 results per clock per SM the special-function unit keeps
+// up with the MMAs, and the polynomial's extra instructions cost more issue slots than they
+// save (measured with 1/2, 1/4, 1/8 and none of the pairs on the FMA pipe: none is fastest).
+constexpr unsigned kPolyPairs = 0x00u;
 
 template <int DP>
 struct FwdLayout {
@@ -508,8 +513,8 @@ __global__ void __launch_bounds__(320, 1)
         }
         const float mb = (m == -INFINITY) ? 0.f : m;
         // exponentials in pairs: x = s * scale * log2(e) - m with one paired FMA, 2^x, the row
-        // sum in 4 paired chains, and the 16-bit pair of P.  In tiles with no masked key a
-        // quarter of the exponentials run on the FMA pipe, the rest on the special-function
+        // sum in 4 paired chains, and the 16-bit pair of P.  In tiles with no masked key the
+        // pairs selected by kPolyPairs run on the FMA pipe, the rest on the special-function
         // unit; masked tiles use the latter only (exact zeros).
         const uint64_t scl = f2_pack(sl2, sl2), nmb = f2_pack(-mb, -mb);
         uint64_t acc[4];
@@ -519,7 +524,7 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 64; c += 2) {
             const uint64_t x = f2_fma(f2_pack(s[c], s[c + 1]), scl, nmb);
             uint64_t e;
-            if (((c >> 1) & 3) == 3) {
+            if ((kPolyPairs >> ((c >> 1) & 7)) & 1) {
               e = exp2_fma2(x);
             } else {
               const float2 xf = f2_unpack(x);
