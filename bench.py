@@ -98,7 +98,7 @@ def workload_flops(wl, lengths=None):
     from exact_attention_50_gb300 import workloads as W
     if wl.varlen:
         f = W.varlen_fwd_flops(lengths, wl.Hq, wl.d, wl.causal)
-        return f, 0.0
+        return f, (2.5 * f if wl.backward else 0.0)
     f = W.fwd_flops(wl.B, wl.Hq, wl.N, wl.d, wl.causal)
     return f, (W.bwd_flops(wl.B, wl.Hq, wl.N, wl.d, wl.causal) if wl.backward else 0.0)
 
@@ -184,6 +184,7 @@ def oracle_sample(wl, seconds: float, seed: int = 0):
     heads of one kv head, one batch) forward + backward, until `seconds` have passed.  Returns
     (TFLOP/s, cores, description)."""
     import numpy as np
+    import torch
     import oracle
     from exact_attention_50_gb300 import workloads as W
     oracle.build()
@@ -193,15 +194,22 @@ def oracle_sample(wl, seconds: float, seed: int = 0):
         qkv, cu, lengths, _ = W.varlen_inputs(wl.varlen, wl.Hq, wl.d, wl.dtype, seed=seed)
         done, flops, t0 = 0, 0.0, time.perf_counter()
         cu_l = cu.tolist()
+        g = torch.Generator().manual_seed(1)
+        dout = torch.randn(qkv.shape[0], wl.Hq, wl.d, generator=g).to(qkv.dtype)
         for s in np.argsort(lengths):
             a, b = cu_l[s], cu_l[s + 1]
             oracle.fwd_varlen(qkv[a:b].double().numpy(), [0, b - a], wl.causal)
             flops += W.fwd_flops(1, wl.Hq, b - a, wl.d, wl.causal)
+            if wl.backward:  # the sequence as a dense [1, H, L, d] problem
+                q, k, v = (qkv[a:b, i].permute(1, 0, 2).unsqueeze(0).double().numpy() for i in range(3))
+                oracle.bwd(q, k, v, dout[a:b].permute(1, 0, 2).unsqueeze(0).double().numpy(), wl.causal)
+                flops += W.bwd_flops(1, wl.Hq, b - a, wl.d, wl.causal)
             done += 1
             if time.perf_counter() - t0 >= seconds:
                 break
         dt = time.perf_counter() - t0
-        return flops / dt / 1e12, cores, f"{done} of {len(lengths)} sequences (shortest first), fwd, fp64"
+        what = "fwd+bwd" if wl.backward else "fwd"
+        return flops / dt / 1e12, cores, f"{done} of {len(lengths)} sequences (shortest first), {what}, fp64"
     G = wl.G
     q, k, v, dout = W.dense_inputs(1, G, 1, wl.N, wl.d, wl.dtype, seed=seed)
     per_group = W.fwd_flops(1, G, wl.N, wl.d, wl.causal) * (3.5 if wl.backward else 1.0)
@@ -268,6 +276,21 @@ def run_ours(args, rank, world, local):
             return lib.attn_fwd_varlen(qkv.data_ptr(), cu.data_ptr(), len(lengths), T, maxlen, out.data_ptr(),
                                        lse.data_ptr(), wl.Hq, wl.d, int(wl.causal), scale, dt_code, 0, sp)
         bwd_calls = []
+        if wl.backward:
+            g = torch.Generator().manual_seed(1)
+            do_h = torch.randn(T, wl.Hq, wl.d, generator=g).to(qkv_h.dtype)
+            dout = do_h.to(dev)
+            dqkv = torch.empty_like(qkv)
+            nbytes = lib.attn_bwd_varlen_workspace_bytes(T, wl.Hq, wl.d)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            host_in.append(do_h)
+            dev_in.append(dout)
+            dev_out.append(dqkv)
+            bwd_calls = [
+                lambda: lib.attn_bwd_varlen(qkv.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                                            cu.data_ptr(), len(lengths), T, maxlen, dqkv.data_ptr(), ws.data_ptr(),
+                                            nbytes, wl.Hq, wl.d, int(wl.causal), scale, dt_code, 0, sp),
+            ]
     else:
         q_h, k_h, v_h, do_h = W.dense_inputs(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.dtype, seed=0,
                                              with_dout=wl.backward)
@@ -394,8 +417,10 @@ def run_ours(args, rank, world, local):
 
     peaks = read_peaks()
     # dominant kernel: the backward main kernel when there is a backward, else the forward
-    if bwd_calls:
+    if len(bwd_calls) == 3:
         dom_name, dom_ms, dom_flops = "bwd_tc_kernel", per_call_ms[2], bwd_f
+    elif bwd_calls:  # one call (varlen): its prepare and finish steps are inside the time
+        dom_name, dom_ms, dom_flops = "bwd_tc_kernel", per_call_ms[1], bwd_f
     else:
         dom_name, dom_ms, dom_flops = "fwd_tc_kernel", per_call_ms[0], fwd_f
     peak = peaks["bf16_tflops_sustained"] if wl.dtype != "f32" else None
@@ -411,9 +436,9 @@ def run_ours(args, rank, world, local):
     if bwd_calls:
         bwd_ms = sum(per_call_ms[1:])
         detail.update({"bwd_ms": bwd_ms, "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12,
-                       "bwd_frac": (bwd_f / (bwd_ms * 1e-3) / 1e12) / peak if peak else None,
-                       "bwd_phase_ms": {"prepare": per_call_ms[1], "main": per_call_ms[2],
-                                        "finish": per_call_ms[3]}})
+                       "bwd_frac": (bwd_f / (bwd_ms * 1e-3) / 1e12) / peak if peak else None})
+        if len(bwd_calls) == 3:
+            detail["bwd_phase_ms"] = {"prepare": per_call_ms[1], "main": per_call_ms[2], "finish": per_call_ms[3]}
 
     line = None
     if rank == 0:
@@ -457,11 +482,21 @@ def run_reference(args, rank, world):
         s = int(np.argmin(lengths))
         a, b = cu.tolist()[s], cu.tolist()[s + 1]
         x = qkv[a:b].double().numpy()
+        import torch
+        g = torch.Generator().manual_seed(1)
+        dout = torch.randn(qkv.shape[0], wl.Hq, wl.d, generator=g).to(qkv.dtype)
+        qd, kd, vd = (qkv[a:b, i].permute(1, 0, 2).unsqueeze(0).double().numpy() for i in range(3))
+        dd = dout[a:b].permute(1, 0, 2).unsqueeze(0).double().numpy()
 
         def step():
             oracle.fwd_varlen(x, [0, b - a], wl.causal)
-            return W.fwd_flops(1, wl.Hq, b - a, wl.d, wl.causal)
-        sample = f"sequence {s} (length {b - a}) of the varlen batch per step, fwd, fp64"
+            f = W.fwd_flops(1, wl.Hq, b - a, wl.d, wl.causal)
+            if wl.backward:
+                oracle.bwd(qd, kd, vd, dd, wl.causal)
+                f += W.bwd_flops(1, wl.Hq, b - a, wl.d, wl.causal)
+            return f
+        sample = (f"sequence {s} (length {b - a}) of the varlen batch per step, "
+                  f"{'fwd+bwd' if wl.backward else 'fwd'}, fp64")
     else:
         q, k, v, dout = W.dense_inputs(1, 1, 1, wl.N, wl.d, wl.dtype, seed=0)
         qn, kn, vn, dn = (t.double().numpy() for t in (q, k, v, dout))

@@ -56,6 +56,10 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_finish.restype = i
         lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, i, u, vp]
         lib.attn_bwd_noalloc.restype = i
+        lib.attn_bwd_varlen_workspace_bytes.argtypes = [i, i, i]
+        lib.attn_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp, vp, ctypes.c_size_t, i, i, i, f, i, u, vp]
+        lib.attn_bwd_varlen.restype = i
         lib.attn_get_device_status.argtypes = [vp]
         lib.attn_get_device_status.restype = i
         lib.attn_status_string.argtypes = [i]
@@ -86,6 +90,16 @@ def attn_fwd_varlen(qkv, cu_seqlens, nseq, total_tokens, max_seqlen, out, lse, H
 
 def attn_bwd_workspace_bytes(B, Hq, N, d) -> int:
     return load().attn_bwd_workspace_bytes(B, Hq, N, d)
+
+
+def attn_bwd_varlen_workspace_bytes(total_tokens, H, d) -> int:
+    return load().attn_bwd_varlen_workspace_bytes(total_tokens, H, d)
+
+
+def attn_bwd_varlen(qkv, out, dout, lse, cu_seqlens, nseq, total_tokens, max_seqlen, dqkv, workspace,
+                    workspace_bytes, H, d, causal, scale, dtype, flags, stream) -> int:
+    return load().attn_bwd_varlen(qkv, out, dout, lse, cu_seqlens, nseq, total_tokens, max_seqlen, dqkv, workspace,
+                                  workspace_bytes, H, d, int(causal), float(scale), dtype, flags, stream)
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, causal, scale,

@@ -120,6 +120,31 @@ def fwd_varlen(qkv, cu_seqlens, max_seqlen: int, causal: bool, scale=None, out_f
     return out, lse
 
 
+def bwd_varlen(qkv, out, lse, dout, cu_seqlens, max_seqlen: int, causal: bool, scale=None, out_f32: bool = False,
+               workspace=None):
+    """Packed varlen backward.  qkv [T,3,H,d], out / dout [T,H,d], lse [H,T] (from fwd_varlen),
+    cu_seqlens int32 [nseq+1] (device).  Returns dqkv [T,3,H,d]."""
+    _require(qkv, "qkv")
+    for t, n in ((out, "out"), (dout, "dout")):
+        _require(t, n, qkv.dtype)
+    _require(lse, "lse", torch.float32)
+    _require(cu_seqlens, "cu_seqlens", torch.int32)
+    T, _, H, d = qkv.shape
+    if out.shape != (T, H, d) or dout.shape != (T, H, d) or lse.shape != (H, T):
+        raise ValueError("out and dout must be [T,H,d], lse [H,T]")
+    nseq = cu_seqlens.numel() - 1
+    dqkv = torch.zeros(qkv.shape, dtype=torch.float32 if out_f32 else qkv.dtype, device=qkv.device)
+    nbytes = _lib.attn_bwd_varlen_workspace_bytes(T, H, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=qkv.device)
+    st = _lib.attn_bwd_varlen(qkv.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(), cu_seqlens.data_ptr(),
+                              nseq, T, int(max_seqlen), dqkv.data_ptr(), workspace.data_ptr(), workspace.numel(), H,
+                              d, causal, _scale_arg(scale), _dtype_code(qkv),
+                              _lib.ATTN_FLAG_OUT_F32 if out_f32 else 0, _stream())
+    _lib._check(st, "attn_bwd_varlen")
+    return dqkv
+
+
 class _AttnFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, causal, scale):
@@ -143,13 +168,16 @@ def flash_attention(q, k, v, causal: bool = True, scale=None):
 class _VarlenFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, qkv, cu_seqlens, max_seqlen, causal, scale):
-        out, _ = fwd_varlen(qkv, cu_seqlens, max_seqlen, causal, scale, with_lse=False)
+        out, lse = fwd_varlen(qkv, cu_seqlens, max_seqlen, causal, scale)
+        ctx.save_for_backward(qkv, out, lse, cu_seqlens)
+        ctx.max_seqlen, ctx.causal, ctx.scale = max_seqlen, causal, scale
         return out
 
     @staticmethod
     def backward(ctx, dout):
-        raise NotImplementedError("the packed varlen backward is not provided; use the dense "
-                                  "flash_attention path for training")
+        qkv, out, lse, cu_seqlens = ctx.saved_tensors
+        dqkv = bwd_varlen(qkv, out, lse, dout.contiguous(), cu_seqlens, ctx.max_seqlen, ctx.causal, ctx.scale)
+        return dqkv, None, None, None, None
 
 
 def flash_attn_varlen_qkvpacked_func(qkv, cu_seqlens, max_seqlen, dropout_p=0.0, softmax_scale=None,

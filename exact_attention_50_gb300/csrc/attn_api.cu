@@ -74,6 +74,16 @@ bool make_dense_map(CUtensorMap* map, const void* base, attn_dtype_t dt, int hea
   return make_map(map, base, dt, 3, dims, strides, box);
 }
 
+// {d, rows, heads} over a [rows, heads, d]-like layout with the given element strides (a plane
+// of packed qkv, or a [T, H, d] tensor): the same box and coordinates as the dense maps.
+bool make_rows_map(CUtensorMap* map, const void* base, attn_dtype_t dt, int rows, int heads, int d,
+                   long long row_stride, long long head_stride) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(rows), static_cast<uint64_t>(heads)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(row_stride) * 2, static_cast<uint64_t>(head_stride) * 2};
+  const uint32_t box[3] = {64, 128, 1};
+  return make_map(map, base, dt, 3, dims, strides, box);
+}
+
 bool make_packed_map(CUtensorMap* map, const void* base, attn_dtype_t dt, int T, int H, int d) {
   const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(H), 3, static_cast<uint64_t>(T)};
   const uint64_t strides[3] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(H) * d * 2,
@@ -186,7 +196,7 @@ namespace {
 
 // Shared validation of the backward's sizes and workspace; fills the common BwdParams fields.
 attn_status_t bwd_setup(BwdParams* p, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
-                        float scale, attn_dtype_t dtype, unsigned flags) {
+                        float scale, attn_dtype_t dtype, unsigned flags, int grid_rows = -1) {
   attn_status_t st = check_common(d, scale, dtype);
   if (st != ATTN_OK) return st;
   if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
@@ -195,12 +205,15 @@ attn_status_t bwd_setup(BwdParams* p, void* workspace, size_t workspace_bytes, i
   if (!workspace || !aligned(workspace, 256)) return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, N, d)) return ATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  if ((N + 31) / 32 > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (((grid_rows < 0 ? N : grid_rows) + 31) / 32 > 65535) return ATTN_ERR_UNSUPPORTED;  // grid y extent
   const size_t rows = static_cast<size_t>(B) * Hq * N;
   p->dq_acc = static_cast<float*>(workspace);
   p->delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * d * sizeof(float)));
   p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->N = N; p->d = d; p->G = Hq / Hkv;
   p->n_ktiles = (N + attn::kBN - 1) / attn::kBN;
+  const BwdParams::Rows dense{d, static_cast<long long>(N) * d};
+  p->lay_q = p->lay_kv = p->lay_o = p->lay_dq = p->lay_dkv = dense;
+  p->cu_seqlens = nullptr;
   p->scale = resolve_scale(scale, d);
   p->scale_log2 = p->scale * kLog2e;
   p->out_f32 = (flags & ATTN_FLAG_OUT_F32) ? 1 : 0;
@@ -273,6 +286,68 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        dtype, flags, stream);
   if (st == ATTN_OK) st = attn_bwd_finish(dq, workspace, workspace_bytes, B, Hq, N, d, scale, dtype, flags, stream);
   return st;
+}
+
+size_t attn_bwd_varlen_workspace_bytes(int total_tokens, int H, int d) {
+  return attn_bwd_workspace_bytes(1, H, total_tokens, d);
+}
+
+attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout, const float* lse,
+                              const int32_t* cu_seqlens, int nseq, int total_tokens, int max_seqlen, void* dqkv,
+                              void* workspace, size_t workspace_bytes, int H, int d, int causal, float scale,
+                              attn_dtype_t dtype, unsigned flags, void* stream) {
+  attn_status_t st = check_common(d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (nseq < 0 || total_tokens < 0 || max_seqlen < 0 || H <= 0) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAG_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (nseq == 0) return total_tokens == 0 ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+  if (!cu_seqlens || !aligned(cu_seqlens, 4)) return ATTN_ERR_INVALID_ARG;
+  if (total_tokens == 0) return ATTN_OK;  // every sequence is empty
+  if (max_seqlen == 0) return ATTN_ERR_INVALID_ARG;
+  if (!all_aligned16({qkv, out, dout, dqkv}) || !lse || !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_varlen_workspace_bytes(total_tokens, H, d)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(nseq) * H > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+
+  // The sequences are the diagonal blocks of a B = 1, N = total_tokens problem with Hq = Hkv = H.
+  BwdParams p{};
+  st = bwd_setup(&p, workspace, workspace_bytes, 1, H, H, total_tokens, d, scale, dtype, flags, max_seqlen);
+  if (st != ATTN_OK) return st;
+  const long long hd = static_cast<long long>(H) * d;
+  const BwdParams::Rows packed{3 * hd, d}, rows{hd, d};
+  p.lay_q = p.lay_kv = p.lay_dq = p.lay_dkv = packed;
+  p.lay_o = rows;
+  p.cu_seqlens = cu_seqlens;
+  p.nseq = nseq;
+  p.max_seqlen = max_seqlen;
+  p.n_ktiles = (max_seqlen + attn::kBN - 1) / attn::kBN;
+  const size_t es = dtype == ATTN_F32 ? 4 : 2;                 // input element size
+  const size_t eo = (dtype == ATTN_F32 || p.out_f32) ? 4 : es;  // output element size
+  const char* in = static_cast<const char*>(qkv);
+  char* outp = static_cast<char*>(dqkv);
+  p.q = in;
+  p.k = in + hd * es;
+  p.v = in + 2 * hd * es;
+  p.o = out;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = outp;
+  p.dk = outp + hd * eo;
+  p.dv = outp + 2 * hd * eo;
+  if (!(p.status = status_word())) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = attn::launch_bwd_preprocess(p, dtype, dtype != ATTN_F32, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dtype == ATTN_F32) return from_cuda(attn::launch_bwd_f32(p, causal != 0, s));
+  BwdMaps maps;
+  if (!make_rows_map(&maps.q, p.q, dtype, total_tokens, H, d, 3 * hd, d) ||
+      !make_rows_map(&maps.k, p.k, dtype, total_tokens, H, d, 3 * hd, d) ||
+      !make_rows_map(&maps.v, p.v, dtype, total_tokens, H, d, 3 * hd, d) ||
+      !make_rows_map(&maps.dout, dout, dtype, total_tokens, H, d, hd, d))
+    return ATTN_ERR_CUDA;
+  e = attn::launch_bwd_tc(maps, p, dtype, causal != 0, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_bwd_postprocess(p, dtype, s));
 }
 
 attn_status_t attn_get_device_status(void* stream) {

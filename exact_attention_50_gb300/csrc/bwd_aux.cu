@@ -30,16 +30,19 @@ __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-template <typename T>
+// Rows are walked in the order of the fp32 statistics (head-major: r = head * N + n); the O and
+// dO row of (head, n) is at head * lay.head + n * lay.row.
+template <typename T, bool CONTIG>
 __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dout,
                                                          float* __restrict__ delta, float* __restrict__ dq_acc,
-                                                         long rows, int d) {
+                                                         long rows, int N, BwdParams::Rows lay, int d) {
   constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte load
   const long warps = static_cast<long>(gridDim.x) * (blockDim.x / 32);
   const int lane = threadIdx.x & 31;
   for (long r = static_cast<long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; r < rows; r += warps) {
-    const T* orow = o + r * d;
-    const T* grow = dout + r * d;
+    const long long ofs = CONTIG ? r * d : (r / N) * lay.head + (r % N) * lay.row;
+    const T* orow = o + ofs;
+    const T* grow = dout + ofs;
     float acc = 0.f;
     for (int c = lane * kVec; c < d; c += 32 * kVec) {
       const uint4 a = *reinterpret_cast<const uint4*>(orow + c);
@@ -59,13 +62,22 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ o
   }
 }
 
-template <typename T, typename OutT>
+// The accumulator is in statistics order ([heads * N, d]); row (head, n) of dQ is at
+// head * lay.head + n * lay.row.
+template <typename OutT, bool CONTIG>
 __global__ void __launch_bounds__(256) postprocess_kernel(const float* __restrict__ acc, OutT* __restrict__ out,
-                                                          long n4, float scale) {
+                                                          long n4, int N, BwdParams::Rows lay, int d, float scale) {
   const long stride = static_cast<long>(gridDim.x) * blockDim.x;
+  const int d4 = d / 4;
   for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
     const float4 a = reinterpret_cast<const float4*>(acc)[i];
-    OutT* dst = out + 4 * i;
+    OutT* dst;
+    if constexpr (CONTIG) {
+      dst = out + 4 * i;
+    } else {
+      const long r = i / d4;
+      dst = out + (r / N) * lay.head + (r % N) * lay.row + 4 * (i % d4);
+    }
     dst[0] = from_f<OutT>(a.x * scale);
     dst[1] = from_f<OutT>(a.y * scale);
     dst[2] = from_f<OutT>(a.z * scale);
@@ -82,24 +94,39 @@ int grid_for(long work, int per_block) {
 
 }  // namespace
 
+namespace {
+bool contiguous(const BwdParams::Rows& lay, const BwdParams& p) {
+  return lay.row == p.d && lay.head == static_cast<long long>(p.N) * p.d;
+}
+
+template <typename T>
+void preprocess_t(const BwdParams& p, float* acc, long rows, int grid, cudaStream_t stream) {
+  const T* o = static_cast<const T*>(p.o);
+  const T* g = static_cast<const T*>(p.dout);
+  if (contiguous(p.lay_o, p))
+    preprocess_kernel<T, true><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, rows, p.N, p.lay_o, p.d);
+  else
+    preprocess_kernel<T, false><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, rows, p.N, p.lay_o, p.d);
+}
+
+template <typename OutT>
+void postprocess_t(const BwdParams& p, long n4, int grid, cudaStream_t stream) {
+  OutT* out = static_cast<OutT*>(p.dq);
+  if (contiguous(p.lay_dq, p))
+    postprocess_kernel<OutT, true><<<grid, 256, 0, stream>>>(p.dq_acc, out, n4, p.N, p.lay_dq, p.d, p.scale);
+  else
+    postprocess_kernel<OutT, false><<<grid, 256, 0, stream>>>(p.dq_acc, out, n4, p.N, p.lay_dq, p.d, p.scale);
+}
+}  // namespace
+
 cudaError_t launch_bwd_preprocess(const BwdParams& p, attn_dtype_t dtype, bool zero_acc, cudaStream_t stream) {
   const long rows = static_cast<long>(p.B) * p.Hq * p.N;
   const int grid = grid_for(rows, 8);
   float* acc = zero_acc ? p.dq_acc : nullptr;
   switch (dtype) {
-    case ATTN_F32:
-      preprocess_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(p.o),
-                                                         static_cast<const float*>(p.dout), p.delta, acc, rows, p.d);
-      break;
-    case ATTN_F16:
-      preprocess_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<const __half*>(p.o),
-                                                          static_cast<const __half*>(p.dout), p.delta, acc, rows, p.d);
-      break;
-    default:
-      preprocess_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(p.o),
-                                                                 static_cast<const __nv_bfloat16*>(p.dout), p.delta,
-                                                                 acc, rows, p.d);
-      break;
+    case ATTN_F32: preprocess_t<float>(p, acc, rows, grid, stream); break;
+    case ATTN_F16: preprocess_t<__half>(p, acc, rows, grid, stream); break;
+    default: preprocess_t<__nv_bfloat16>(p, acc, rows, grid, stream); break;
   }
   return cudaGetLastError();
 }
@@ -108,12 +135,11 @@ cudaError_t launch_bwd_postprocess(const BwdParams& p, attn_dtype_t dtype, cudaS
   const long n4 = static_cast<long>(p.B) * p.Hq * p.N * p.d / 4;
   const int grid = grid_for(n4, 256);
   if (p.out_f32)
-    postprocess_kernel<float, float><<<grid, 256, 0, stream>>>(p.dq_acc, static_cast<float*>(p.dq), n4, p.scale);
+    postprocess_t<float>(p, n4, grid, stream);
   else if (dtype == ATTN_F16)
-    postprocess_kernel<__half, __half><<<grid, 256, 0, stream>>>(p.dq_acc, static_cast<__half*>(p.dq), n4, p.scale);
+    postprocess_t<__half>(p, n4, grid, stream);
   else
-    postprocess_kernel<__nv_bfloat16, __nv_bfloat16>
-        <<<grid, 256, 0, stream>>>(p.dq_acc, static_cast<__nv_bfloat16*>(p.dq), n4, p.scale);
+    postprocess_t<__nv_bfloat16>(p, n4, grid, stream);
   return cudaGetLastError();
 }
 

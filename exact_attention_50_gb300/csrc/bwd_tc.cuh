@@ -126,10 +126,31 @@ __global__ void __launch_bounds__(512, 1)
   // Blocks are dispatched in linear order (x fastest): every (batch, kv head) of key tile 0,
   // the heaviest under the causal mask, then key tile 1, ...; each SM that frees up takes the
   // heaviest tile left, which keeps the causal tail short.
+  // Dense: x = batch * kv head.  Varlen: x = sequence * head; the sequence is the diagonal block
+  // [seq_start, seq_start + seq_len) of a B = 1, N = total_tokens problem (G = 1).
   const int kt = blockIdx.y;
-  const int b = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
+  int hkv, hq0, seq_start = 0, seq_len = p.N;  // kv head (row block), its first query head, sequence
+  if (p.cu_seqlens) {
+    const int s = blockIdx.x / p.Hkv, hh = blockIdx.x % p.Hkv;
+    const int c0 = p.cu_seqlens[s], c1 = p.cu_seqlens[s + 1];
+    const bool bad = c0 < 0 || c1 < c0 || c1 > p.N || c1 - c0 > p.max_seqlen || (s == 0 && c0 != 0) ||
+                     (s == p.nseq - 1 && c1 != p.N);
+    if (bad) {
+      if (threadIdx.x == 0 && kt == 0 && hh == 0) raise_status(p.status, ATTN_ERR_DEVICE_INPUT);
+      return;  // the whole CTA, before any barrier or allocation
+    }
+    seq_start = c0;
+    seq_len = c1 - c0;
+    hkv = hh;
+    hq0 = hh * p.G;
+  } else {
+    const int b = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
+    hkv = b * p.Hkv + g;
+    hq0 = b * p.Hq + g * p.G;
+  }
   const int N = p.N;
-  const int n_q = (N + kBM - 1) / kBM;
+  const int n_q = (seq_len + kBM - 1) / kBM;
+  if (kt >= n_q) return;  // a key tile past this sequence's end (varlen): the whole CTA
   const int qt0 = CAUSAL ? kt : 0;
   const int per_head = n_q - qt0;
   const int n_it = p.G * per_head;
@@ -172,26 +193,26 @@ __global__ void __launch_bounds__(512, 1)
       tma_prefetch_desc(&tmdO);
       mbar_expect_tx(kv_full, 2 * L::kTileBytes);
       for (int c = 0; c < kChunks; ++c) {
-        tma_load_3d(sK + c * L::kChunkBytes, &tmK, kv_full, c * 64, kt * kBN, b * p.Hkv + g);
-        tma_load_3d(sV + c * L::kChunkBytes, &tmV, kv_full, c * 64, kt * kBN, b * p.Hkv + g);
+        tma_load_3d(sK + c * L::kChunkBytes, &tmK, kv_full, c * 64, seq_start + kt * kBN, hkv);
+        tma_load_3d(sV + c * L::kChunkBytes, &tmV, kv_full, c * 64, seq_start + kt * kBN, hkv);
       }
       int nq_issued = 0, ndo_issued = 0;
       for (int it = 0; it < n_it; ++it) {
-        const int h = g * p.G + it / per_head, qt = qt0 + it % per_head;
+        const int hq = hq0 + it / per_head, qt = qt0 + it % per_head;
         const int st = it % QS;
         const uint32_t ph = ((it / QS) - 1) & 1;
         // dO first: its slot frees earlier (after dV)
         if (it >= QS && !mbar_wait(do_empty + st, ph, abort_flag, p.status)) break;
         mbar_expect_tx(do_full + st, L::kTileBytes);
         for (int c = 0; c < kChunks; ++c)
-          tma_load_3d(sdO + st * L::kTileBytes + c * L::kChunkBytes, &tmdO, do_full + st, c * 64, qt * kBM,
-                      b * p.Hq + h);
+          tma_load_3d(sdO + st * L::kTileBytes + c * L::kChunkBytes, &tmdO, do_full + st, c * 64,
+                      seq_start + qt * kBM, hq);
         ndo_issued = it + 1;
         if (it >= QS && !mbar_wait(q_empty + st, ph, abort_flag, p.status)) break;
         mbar_expect_tx(q_full + st, L::kTileBytes);
         for (int c = 0; c < kChunks; ++c)
-          tma_load_3d(sQ + st * L::kTileBytes + c * L::kChunkBytes, &tmQ, q_full + st, c * 64, qt * kBM,
-                      b * p.Hq + h);
+          tma_load_3d(sQ + st * L::kTileBytes + c * L::kChunkBytes, &tmQ, q_full + st, c * 64,
+                      seq_start + qt * kBM, hq);
         nq_issued = it + 1;
       }
       if (abort_read(abort_flag)) {
@@ -310,8 +331,8 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int h = g * p.G + it / per_head, qt = qt0 + it % per_head;
-      const size_t row_base = (static_cast<size_t>(b) * p.Hq + h) * N;
+      const int qt = qt0 + it % per_head;
+      const size_t row_base = static_cast<size_t>(hq0 + it / per_head) * N + seq_start;
       if (!mbar_wait_warp(dq_full, it & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const int q = qt * kBM + t;
@@ -328,7 +349,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_before();
           mbar_arrive_warp(dq_free);  // the dQ columns may be overwritten once everything is loaded
         }
-        if (q < N) {
+        if (q < seq_len) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int col = c2 * 64 + i * 4;
@@ -350,7 +371,7 @@ __global__ void __launch_bounds__(512, 1)
     if (ok && mbar_wait_warp(dkdv_done, 0, abort_flag, p.status)) {
       tc_fence_after();
       const int key = kt * kBN + t;
-      const size_t krow = (static_cast<size_t>(b) * p.Hkv + g) * N + key;
+      const long long kofs = hkv * p.lay_dkv.head + (seq_start + key) * p.lay_dkv.row;  // row start
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? L::kColdK : L::kColdV;
@@ -362,17 +383,17 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld32(tl + col + c * 32, r);
           tmem_ld_wait();
           tmem_reg_fence(r);
-          if (key < N && c * 32 < p.d) {
+          if (key < seq_len && c * 32 < p.d) {
             const int ncol = min(32, p.d - c * 32);
             if (p.out_f32) {
-              float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + krow * p.d + c * 32);
+              float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + kofs + c * 32);
 #pragma unroll
               for (int i = 0; i < 8; ++i)
                 if (i * 4 < ncol)
                   o4[i] = make_float4(__uint_as_float(r[4 * i]) * mul, __uint_as_float(r[4 * i + 1]) * mul,
                                       __uint_as_float(r[4 * i + 2]) * mul, __uint_as_float(r[4 * i + 3]) * mul);
             } else {
-              uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(out) + krow * p.d + c * 32);
+              uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(out) + kofs + c * 32);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 if (i * 8 < ncol) {
@@ -396,17 +417,17 @@ __global__ void __launch_bounds__(512, 1)
     const int t = quad * 32 + lane;           // TMEM lane: key row
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int key = kt * kBN + t;
-    const bool key_ok = key < N;
+    const bool key_ok = key < seq_len;
     const float sl2 = p.scale_log2;
     // row terms of tile `it`, loaded one tile ahead by threads 0..127
     float lse_next = 0.f, d_next = 0.f;
     auto load_rows = [&](int it) {
       if (threadIdx.x < 128 && it < n_it) {
-        const int h = g * p.G + it / per_head, qt = qt0 + it % per_head;
-        const size_t row_base = (static_cast<size_t>(b) * p.Hq + h) * N;
+        const int qt = qt0 + it % per_head;
+        const size_t row_base = static_cast<size_t>(hq0 + it / per_head) * N + seq_start;
         const int q = qt * kBM + threadIdx.x;
-        lse_next = q < N ? p.lse[row_base + q] * 1.4426950408889634f : INFINITY;
-        d_next = q < N ? p.delta[row_base + q] : 0.f;
+        lse_next = q < seq_len ? p.lse[row_base + q] * 1.4426950408889634f : INFINITY;
+        d_next = q < seq_len ? p.delta[row_base + q] : 0.f;
       }
     };
     load_rows(0);
@@ -507,7 +528,7 @@ cudaError_t launch_bwd_tc_t(const BwdMaps& maps, const BwdParams& p, cudaStream_
   e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs != static_cast<int>(L::kLaunchRegs)) return cudaErrorInvalidConfiguration;
-  const dim3 grid(p.B * p.Hkv, p.n_ktiles);
+  const dim3 grid(p.cu_seqlens ? p.nseq * p.Hkv : p.B * p.Hkv, p.n_ktiles);
   kern<<<grid, L::kThreads, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, maps.dout, p);
   return cudaGetLastError();
 }

@@ -53,8 +53,21 @@ struct BwdParams {
   int n_ktiles;
   float scale, scale_log2;
   int out_f32;
+  // Element offset of row n of head hh in a [rows, d] tensor: hh * head + n * row (a packed
+  // tensor's plane is part of its pointer).  Dense [B,H,N,d]: {d, N*d} with hh = b*H + h.
+  // Varlen: {token stride, d} with hh = h.
+  struct Rows {
+    long long row, head;
+  };
+  Rows lay_q, lay_kv, lay_o, lay_dq, lay_dkv;  // q; k and v; o and dout; dq; dk and dv
+  // Varlen: the sequences are the diagonal blocks of a B = 1, N = total_tokens problem; the
+  // fp32 row statistics (LSE, D) and the dQ accumulator are [H, T] ([H, T, d]).
+  const int32_t* cu_seqlens;  // null for dense
+  int nseq, max_seqlen;
 };
 
+// Tensor maps for the tcgen05 backward: 3-D {d, rows, heads} with the layout's row / head
+// strides and a {64, 128, 1} box, for dense and varlen tensors alike.
 struct BwdMaps {
   CUtensorMap q, k, v, dout;
 };
@@ -62,7 +75,7 @@ struct BwdMaps {
 cudaError_t launch_bwd_preprocess(const BwdParams& p, attn_dtype_t dtype, bool zero_acc, cudaStream_t stream);
 cudaError_t launch_bwd_postprocess(const BwdParams& p, attn_dtype_t dtype, cudaStream_t stream);
 cudaError_t launch_bwd_tc(const BwdMaps& maps, const BwdParams& p, attn_dtype_t dtype, bool causal,
-                          cudaStream_t stream);
+                          cudaStream_t stream);  // varlen when p.cu_seqlens is set
 cudaError_t launch_bwd_f32(const BwdParams& p, bool causal, cudaStream_t stream);
 
 }  // namespace attn

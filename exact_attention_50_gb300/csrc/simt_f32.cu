@@ -162,6 +162,35 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(const float* __restrict__ 
   }
 }
 
+// Which (kv head, sequence) block x of the backward grid covers: dense x = batch * kv head
+// (the whole sequence), varlen x = sequence * head (a diagonal block of a B = 1 problem).
+struct BwdBlock {
+  int hq0, hkv, seq_start, L;
+  bool ok;
+};
+__device__ __forceinline__ BwdBlock bwd_block(const BwdParams& p, int x) {
+  BwdBlock r{0, 0, 0, p.N, true};
+  if (p.cu_seqlens) {
+    const int s = x / p.Hkv, hh = x % p.Hkv;
+    const int c0 = p.cu_seqlens[s], c1 = p.cu_seqlens[s + 1];
+    if (c0 < 0 || c1 < c0 || c1 > p.N || c1 - c0 > p.max_seqlen || (s == 0 && c0 != 0) ||
+        (s == p.nseq - 1 && c1 != p.N)) {
+      if (threadIdx.x == 0 && blockIdx.y == 0 && hh == 0) raise_status(p.status, ATTN_ERR_DEVICE_INPUT);
+      r.ok = false;
+      return r;
+    }
+    r.seq_start = c0;
+    r.L = c1 - c0;
+    r.hkv = hh;
+    r.hq0 = hh * p.G;
+  } else {
+    const int b = x / p.Hkv, g = x % p.Hkv;
+    r.hkv = b * p.Hkv + g;
+    r.hq0 = b * p.Hq + g * p.G;
+  }
+  return r;
+}
+
 // ------------------------------------------------------------------ backward: dQ
 template <bool CAUSAL>
 __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const BwdParams p) {
@@ -176,15 +205,22 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const BwdParams p) {
   const float* v = static_cast<const float*>(p.v);
   const float* dout = static_cast<const float*>(p.dout);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq, g = h / p.G, d = p.d, N = p.N;
+  // blockIdx.x = (kv block) * G + query head within the group
+  const BwdBlock bb = bwd_block(p, blockIdx.x / p.G);
+  if (!bb.ok) return;
+  const int hq = bb.hq0 + blockIdx.x % p.G, d = p.d, N = bb.L, s0 = bb.seq_start;
   const int row0 = blockIdx.y * kRows;
-  const size_t qbase = (static_cast<size_t>(b) * p.Hq + h) * N;
-  const size_t kbase = (static_cast<size_t>(b) * p.Hkv + g) * N * d;
+  if (row0 >= N) return;  // past this sequence's end (varlen)
+  const size_t qbase = static_cast<size_t>(hq) * p.N + s0;  // row statistics of this head
+  const float* qh = q + hq * p.lay_q.head + s0 * p.lay_q.row;
+  const float* doh = dout + hq * p.lay_o.head + s0 * p.lay_o.row;
+  const float* kh = k + bb.hkv * p.lay_kv.head + s0 * p.lay_kv.row;
+  const float* vh = v + bb.hkv * p.lay_kv.head + s0 * p.lay_kv.row;
   for (int idx = threadIdx.x; idx < kRows * d; idx += blockDim.x) {
     const int r = idx / d, c = idx % d;
     const bool in = row0 + r < N;
-    sQ[r * d + c] = in ? q[(qbase + row0 + r) * d + c] : 0.f;
-    sdO[r * d + c] = in ? dout[(qbase + row0 + r) * d + c] : 0.f;
+    sQ[r * d + c] = in ? qh[(row0 + r) * p.lay_q.row + c] : 0.f;
+    sdO[r * d + c] = in ? doh[(row0 + r) * p.lay_o.row + c] : 0.f;
   }
   float lse2[8], Dr[8], acc[8][kColsPerLane];
 #pragma unroll
@@ -201,8 +237,8 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const BwdParams p) {
     for (int idx = threadIdx.x; idx < kTile * d; idx += blockDim.x) {
       const int r = idx / d, c = idx % d;
       const bool in = key0 + r < N;
-      sK[r * dp1 + c] = in ? k[kbase + static_cast<size_t>(key0 + r) * d + c] : 0.f;
-      sV[r * dp1 + c] = in ? v[kbase + static_cast<size_t>(key0 + r) * d + c] : 0.f;
+      sK[r * dp1 + c] = in ? kh[(key0 + r) * p.lay_kv.row + c] : 0.f;
+      sV[r * dp1 + c] = in ? vh[(key0 + r) * p.lay_kv.row + c] : 0.f;
     }
     __syncthreads();
     const int key = key0 + lane;
@@ -227,7 +263,7 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const BwdParams p) {
       }
     }
   }
-  float* dq = static_cast<float*>(p.dq);
+  float* dq = static_cast<float*>(p.dq) + hq * p.lay_dq.head + s0 * p.lay_dq.row;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const int qrow = row0 + warp * 8 + r;
@@ -235,7 +271,7 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const BwdParams p) {
 #pragma unroll
     for (int i = 0; i < kColsPerLane; ++i) {
       const int c = lane + 32 * i;
-      if (c < d) dq[(qbase + qrow) * d + c] = acc[r][i] * p.scale;
+      if (c < d) dq[qrow * p.lay_dq.row + c] = acc[r][i] * p.scale;
     }
   }
 }
@@ -256,14 +292,18 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const BwdParams p) {
   const float* v = static_cast<const float*>(p.v);
   const float* dout = static_cast<const float*>(p.dout);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv, d = p.d, N = p.N;
+  const BwdBlock bb = bwd_block(p, blockIdx.x);
+  if (!bb.ok) return;
+  const int d = p.d, N = bb.L, s0 = bb.seq_start;
   const int key0 = blockIdx.y * kRows;
-  const size_t kbase = (static_cast<size_t>(b) * p.Hkv + g) * N;
+  if (key0 >= N) return;  // past this sequence's end (varlen)
+  const float* kh = k + bb.hkv * p.lay_kv.head + s0 * p.lay_kv.row;
+  const float* vh = v + bb.hkv * p.lay_kv.head + s0 * p.lay_kv.row;
   for (int idx = threadIdx.x; idx < kRows * d; idx += blockDim.x) {
     const int r = idx / d, c = idx % d;
     const bool in = key0 + r < N;
-    sK[r * d + c] = in ? k[(kbase + key0 + r) * d + c] : 0.f;
-    sV[r * d + c] = in ? v[(kbase + key0 + r) * d + c] : 0.f;
+    sK[r * d + c] = in ? kh[(key0 + r) * p.lay_kv.row + c] : 0.f;
+    sV[r * d + c] = in ? vh[(key0 + r) * p.lay_kv.row + c] : 0.f;
   }
   float dk[8][kColsPerLane], dv[8][kColsPerLane];
 #pragma unroll
@@ -271,15 +311,17 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const BwdParams p) {
 #pragma unroll
     for (int i = 0; i < kColsPerLane; ++i) dk[r][i] = dv[r][i] = 0.f;
   for (int hh = 0; hh < p.G; ++hh) {
-    const int h = g * p.G + hh;
-    const size_t qbase = (static_cast<size_t>(b) * p.Hq + h) * N;
+    const int hq = bb.hq0 + hh;
+    const size_t qbase = static_cast<size_t>(hq) * p.N + s0;  // row statistics of this head
+    const float* qh = q + hq * p.lay_q.head + s0 * p.lay_q.row;
+    const float* doh = dout + hq * p.lay_o.head + s0 * p.lay_o.row;
     for (int qrow0 = CAUSAL ? (key0 / kTile) * kTile : 0; qrow0 < N; qrow0 += kTile) {
       __syncthreads();
       for (int idx = threadIdx.x; idx < kTile * d; idx += blockDim.x) {
         const int r = idx / d, c = idx % d;
         const bool in = qrow0 + r < N;
-        sQ[r * dp1 + c] = in ? q[(qbase + qrow0 + r) * d + c] : 0.f;
-        sdO[r * dp1 + c] = in ? dout[(qbase + qrow0 + r) * d + c] : 0.f;
+        sQ[r * dp1 + c] = in ? qh[(qrow0 + r) * p.lay_q.row + c] : 0.f;
+        sdO[r * dp1 + c] = in ? doh[(qrow0 + r) * p.lay_o.row + c] : 0.f;
       }
       if (threadIdx.x < kTile) {
         const bool in = qrow0 + threadIdx.x < N;
@@ -314,8 +356,8 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const BwdParams p) {
       }
     }
   }
-  float* dkp = static_cast<float*>(p.dk);
-  float* dvp = static_cast<float*>(p.dv);
+  float* dkp = static_cast<float*>(p.dk) + bb.hkv * p.lay_dkv.head + s0 * p.lay_dkv.row;
+  float* dvp = static_cast<float*>(p.dv) + bb.hkv * p.lay_dkv.head + s0 * p.lay_dkv.row;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const int key = key0 + warp * 8 + r;
@@ -324,8 +366,8 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const BwdParams p) {
     for (int i = 0; i < kColsPerLane; ++i) {
       const int c = lane + 32 * i;
       if (c < d) {
-        dkp[(kbase + key) * d + c] = dk[r][i] * p.scale;
-        dvp[(kbase + key) * d + c] = dv[r][i];
+        dkp[key * p.lay_dkv.row + c] = dk[r][i] * p.scale;
+        dvp[key * p.lay_dkv.row + c] = dv[r][i];
       }
     }
   }
@@ -359,8 +401,11 @@ cudaError_t launch_fwd_f32(const void* q, const void* k, const void* v, const Fw
 }
 
 cudaError_t launch_bwd_f32(const BwdParams& p, bool causal, cudaStream_t stream) {
-  const dim3 gq(p.B * p.Hq, (p.N + kRows - 1) / kRows);
-  const dim3 gk(p.B * p.Hkv, (p.N + kRows - 1) / kRows);
+  // dense: x = batch * heads; varlen: x = sequence * heads, y over the longest sequence
+  const int xs = p.cu_seqlens ? p.nseq : p.B;
+  const int ny = ((p.cu_seqlens ? p.max_seqlen : p.N) + kRows - 1) / kRows;
+  const dim3 gq(xs * p.Hq, ny);
+  const dim3 gk(xs * p.Hkv, ny);
   const size_t smem_q = sizeof(float) * (2 * kTile * (p.d + 1) + 2 * kRows * p.d);
   const size_t smem_k = sizeof(float) * (2 * kTile * (p.d + 1) + 2 * kRows * p.d + 2 * kTile);
   auto kq = causal ? bwd_dq_f32_kernel<true> : bwd_dq_f32_kernel<false>;

@@ -54,6 +54,9 @@ WORKLOADS = {
                          Hq=32, Hkv=8, N=2048, d=128, causal=True, scale=None, backward=True),
     "varlen_bf16": Workload("varlen_bf16 16 seqs L~U[64,4096] H16 d128 bf16 causal fwd", "bf16",
                             Hq=16, Hkv=16, d=128, causal=True, scale=None, varlen=(16, 64, 4096)),
+    "varlen_bf16_train": Workload("varlen_bf16_train 16 seqs L~U[64,4096] H16 d128 bf16 causal fwd+bwd", "bf16",
+                                  Hq=16, Hkv=16, d=128, causal=True, scale=None, varlen=(16, 64, 4096),
+                                  backward=True),
     "long_bf16": Workload("long_bf16 B1 Hq32 Hkv8 N32768 d128 bf16 causal fwd+bwd", "bf16", B=1,
                           Hq=32, Hkv=8, N=32768, d=128, causal=True, scale=None, backward=True),
 }

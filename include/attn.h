@@ -128,6 +128,31 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
 attn_status_t attn_bwd_finish(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int N, int d,
                               float scale, attn_dtype_t dtype, unsigned flags, void* stream);
 
+/* Bytes of device workspace attn_bwd_varlen needs (an fp32 dQ accumulator [H, total_tokens, d]
+ * and the fp32 row terms [H, total_tokens], each 256-byte aligned). */
+size_t attn_bwd_varlen_workspace_bytes(int total_tokens, int H, int d);
+
+/*
+ * Backward of attn_fwd_varlen (the training side of flash_attn_varlen_qkvpacked_func, per the
+ * Turing varlen article's packed layout; the recompute follows the FlashAttention-T review,
+ * FAQ 4).  Each sequence is differentiated on its own, as attn_bwd would for a batch of one.
+ *   qkv, cu_seqlens, nseq, total_tokens, max_seqlen, H, d, causal, scale, dtype: as given to
+ *               attn_fwd_varlen
+ *   out, lse    its output [total_tokens, H, d] (dtype) and LSE [H, total_tokens] float32
+ *   dout        dL/dout [total_tokens, H, d] (dtype)
+ *   dqkv        [total_tokens, 3, H, d]: plane 0 = dq, 1 = dk, 2 = dv (dtype, or float32 with
+ *               ATTN_FLAG_OUT_F32); rows of zero-length sequences are not written
+ *   workspace   DEVICE, at least attn_bwd_varlen_workspace_bytes(total_tokens, H, d) bytes,
+ *               256-byte aligned; contents on entry are ignored, on exit undefined.
+ * Argument errors return a status before any launch; a cu_seqlens array that is not
+ * non-decreasing from 0 or a sequence longer than max_seqlen is detected on the device: the
+ * affected work is skipped and attn_get_device_status() returns ATTN_ERR_DEVICE_INPUT.
+ */
+attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout, const float* lse,
+                              const int32_t* cu_seqlens, int nseq, int total_tokens, int max_seqlen, void* dqkv,
+                              void* workspace, size_t workspace_bytes, int H, int d, int causal, float scale,
+                              attn_dtype_t dtype, unsigned flags, void* stream);
+
 /*
  * attn_bwd_noalloc -- the backward (same arguments, layouts and results as attn_bwd) for callers
  * that cannot allocate device memory when they call it: for example a plugin or host program

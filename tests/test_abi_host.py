@@ -131,3 +131,28 @@ def test_python_wrapper_rejects_unsupported_flags():
             flash_attn_varlen_qkvpacked_func(qkv, cu, 7, **kw)
     with pytest.raises(ValueError, match="Token count mismatch"):
         flash_attn_varlen_qkvpacked_func(torch.zeros(11, 3, 2, 64), cu, 7)
+
+
+def test_bwd_varlen_workspace_and_validation(lib):
+    T, H, d = 300, 2, 64
+    ws = _lib.attn_bwd_varlen_workspace_bytes(T, H, d)
+    assert ws == _lib.attn_bwd_workspace_bytes(1, H, T, d)
+    f = lambda **kw: _lib.attn_bwd_varlen(kw.get("qkv", 4096), kw.get("out", 4096), kw.get("dout", 4096),
+                                          kw.get("lse", 4096), kw.get("cu", 4096), kw.get("nseq", 2),
+                                          kw.get("T", T), kw.get("maxlen", 200), kw.get("dqkv", 4096),
+                                          kw.get("ws", 4096), kw.get("wsb", ws), kw.get("H", H), kw.get("d", d),
+                                          0, 0.0, _lib.ATTN_BF16, kw.get("flags", 0), None)
+    assert f(nseq=-1) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(nseq=0, T=0) == _lib.ATTN_OK
+    assert f(nseq=0, T=3) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(T=0) == _lib.ATTN_OK
+    assert f(cu=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(maxlen=0) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(dqkv=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(lse=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(dout=4100) == _lib.ATTN_ERR_INVALID_ARG   # not 16-byte aligned
+    assert f(ws=4096 + 128) == _lib.ATTN_ERR_INVALID_ARG  # not 256-byte aligned
+    assert f(wsb=ws - 1) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(H=0) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(d=40) == _lib.ATTN_ERR_UNSUPPORTED
+    assert f(flags=2) == _lib.ATTN_ERR_INVALID_ARG
