@@ -67,6 +67,20 @@ bool make_map(CUtensorMap* map, const void* base, attn_dtype_t dt, int rank, con
   return r == CUDA_SUCCESS;
 }
 
+// The fp32 dQ accumulator [rows, d] as a 2-D map with a {32, 128} box (128 bytes per row).
+bool make_acc_map(CUtensorMap* map, const float* base, long long rows, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(d) * 4};
+  const uint32_t box[2] = {32, 128};
+  const uint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_dense_map(CUtensorMap* map, const void* base, attn_dtype_t dt, int heads_total, int N, int d) {
   const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(N), static_cast<uint64_t>(heads_total)};
   const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(N) * d * 2};
@@ -256,7 +270,8 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
   if (dtype == ATTN_F32) return from_cuda(attn::launch_bwd_f32(p, causal != 0, s));
   BwdMaps maps;
   if (!make_dense_map(&maps.q, q, dtype, B * Hq, N, d) || !make_dense_map(&maps.k, k, dtype, B * Hkv, N, d) ||
-      !make_dense_map(&maps.v, v, dtype, B * Hkv, N, d) || !make_dense_map(&maps.dout, dout, dtype, B * Hq, N, d))
+      !make_dense_map(&maps.v, v, dtype, B * Hkv, N, d) || !make_dense_map(&maps.dout, dout, dtype, B * Hq, N, d) ||
+      !make_acc_map(&maps.dq_acc, p.dq_acc, static_cast<long long>(B) * Hq * N, d))
     return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_bwd_tc(maps, p, dtype, causal != 0, s));
 }
@@ -343,7 +358,8 @@ attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout
   if (!make_rows_map(&maps.q, p.q, dtype, total_tokens, H, d, 3 * hd, d) ||
       !make_rows_map(&maps.k, p.k, dtype, total_tokens, H, d, 3 * hd, d) ||
       !make_rows_map(&maps.v, p.v, dtype, total_tokens, H, d, 3 * hd, d) ||
-      !make_rows_map(&maps.dout, dout, dtype, total_tokens, H, d, hd, d))
+      !make_rows_map(&maps.dout, dout, dtype, total_tokens, H, d, hd, d) ||
+      !make_acc_map(&maps.dq_acc, p.dq_acc, static_cast<long long>(H) * total_tokens, d))
     return ATTN_ERR_CUDA;
   e = attn::launch_bwd_tc(maps, p, dtype, causal != 0, s);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;

@@ -48,8 +48,8 @@ struct BwdLayout {
   static constexpr int kOffRow = kOffdSl + 2 * kChunkBytes;        // LSE*log2e and D, 2 buffers each
   static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
   // kv_full, q_full[QS], q_empty[QS], do_full[QS], do_empty[QS], s_full, dp_full, p_full,
-  // dv_done, ds_full, ds_free, dq_full, dq_free, dkdv_done, rows_ready, drain
-  static constexpr int kNumBars = 1 + 4 * kQStages + 11;
+  // dv_done, ds_full, stage_free, dq_full, dq_free, dkdv_done, rows_ready, stage_full, drain
+  static constexpr int kNumBars = 1 + 4 * kQStages + 12;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;
@@ -87,7 +87,7 @@ template <typename T, int DP, bool CAUSAL>
 __global__ void __launch_bounds__(512, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmAcc, const BwdParams p) {
   using L = BwdLayout<DP>;
   constexpr int QS = L::kQStages;
   constexpr int kChunks = DP / 64;
@@ -113,12 +113,14 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* p_full = dp_full + 1;
   uint64_t* dv_done = p_full + 1;
   uint64_t* ds_full = dv_done + 1;
-  uint64_t* ds_free = ds_full + 1;
-  uint64_t* dq_full = ds_free + 1;
+  // the dS area is reused to stage dQ tiles: free once the tile's reduction has read it
+  uint64_t* stage_free = ds_full + 1;
+  uint64_t* dq_full = stage_free + 1;
   uint64_t* dq_free = dq_full + 1;
   uint64_t* dkdv_done = dq_free + 1;
   uint64_t* rows_ready = dkdv_done + 1;  // the 128 row terms (LSE, D) of the current tile are in smem
-  uint64_t* drain = rows_ready + 1;
+  uint64_t* stage_full = rows_ready + 1;  // the read-out warps have staged the dQ tile
+  uint64_t* drain = stage_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
@@ -168,11 +170,12 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(p_full, kEw / 32);  // one arrival per warp
     mbar_init(dv_done, 1);
     mbar_init(ds_full, kEw / 32);
-    mbar_init(ds_free, 1);
+    mbar_init(stage_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);
     mbar_init(dkdv_done, 1);
     mbar_init(rows_ready, kEw / 32);
+    mbar_init(stage_full, 4);
     mbar_init(drain, 1);
     abort_set(abort_flag, 0);
     mbar_init_fence();
@@ -313,7 +316,6 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
         mma_commit(dq_full);
-        mma_commit(ds_free);
       }
       if (ok) {
         mma_commit(dkdv_done);
@@ -330,43 +332,50 @@ __global__ void __launch_bounds__(512, 1)
     const int t = quad * 32 + lane;  // TMEM lane: query row of dQ, key row of dK / dV
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
+    // dQ_t goes from TMEM into the dS area of shared memory (free: the dK and dQ MMAs that read
+    // dS have completed when dq_full arrives), in the 128-byte swizzled layout of the
+    // accumulator map's {32, 128} box, chunk c of 32 columns at c * 16 KB; the TMEM columns are
+    // released at once, and one thread adds the staged tile into the fp32 accumulator with
+    // tile reductions.  Rows of the tile past the sequence hold exact zeros (P = 0 there), so
+    // they add nothing; rows past the accumulator are skipped by the map.
+    uint8_t* stage = sdSh;
     for (int it = 0; it < n_it; ++it) {
       const int qt = qt0 + it % per_head;
-      const size_t row_base = static_cast<size_t>(hq0 + it / per_head) * N + seq_start;
+      const int row0 = static_cast<int>(static_cast<size_t>(hq0 + it / per_head) * N + seq_start) + qt * kBM;
       if (!mbar_wait_warp(dq_full, it & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      const int q = qt * kBM + t;
-      float* dst = p.dq_acc + (row_base + q) * static_cast<size_t>(p.d);
-#pragma unroll
-      for (int c2 = 0; c2 < DP / 64; ++c2) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tl + L::kColdQ + c2 * 64, r0);
-        tmem_ld32(tl + L::kColdQ + c2 * 64 + 32, r1);
+#pragma unroll 1
+      for (int c = 0; c < DP / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + L::kColdQ + c * 32, r);
         tmem_ld_wait();
-        tmem_reg_fence(r0);
-        tmem_reg_fence(r1);
-        if (c2 == DP / 64 - 1) {
+        tmem_reg_fence(r);
+        if (c == DP / 32 - 1) {
           tc_fence_before();
           mbar_arrive_warp(dq_free);  // the dQ columns may be overwritten once everything is loaded
         }
-        if (q < seq_len) {
+        uint8_t* row = stage + c * 16384 + t * 128;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = c2 * 64 + i * 4;
-            if (col < p.d)
-              red_add_v4(dst + col, __uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
-                         __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
-          }
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<uint4*>(row + ((g ^ (t & 7)) << 4)) = make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]);
+      }
+      fence_async_smem();
+      mbar_arrive_warp(stage_full);
+      if (warp == 8 && lane == 0) {
+        if (!mbar_wait(stage_full, it & 1, abort_flag, p.status)) { ok = false; }
+        if (ok) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = c2 * 64 + 32 + i * 4;
-            if (col < p.d)
-              red_add_v4(dst + col, __uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]),
-                         __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]));
-          }
+          for (int c = 0; c < DP / 32; ++c)
+            if (c * 32 < p.d) tma_reduce_add_2d(&tmAcc, stage + c * 16384, c * 32, row0);
+          bulk_commit();
+          bulk_wait_read();
+          mbar_arrive(stage_free);  // the dS area may take the next tile's dS
         }
       }
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, ok)) break;
     }
+    if (warp == 8 && lane == 0) bulk_wait_all();  // the reductions complete before the CTA ends
     // ---- epilogue: dK (scaled) and dV rows of this key tile
     if (ok && mbar_wait_warp(dkdv_done, 0, abort_flag, p.status)) {
       tc_fence_after();
@@ -475,7 +484,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_arrive_warp(p_full);
       load_rows(it + 1);  // prefetch the next tile's LSE and D
       // ---- phase 2: dS^T = P^T (dP^T - D), hi/lo into shared memory
-      if (it >= 1 && !mbar_wait_warp(ds_free, (it - 1) & 1, abort_flag, p.status)) break;
+      if (it >= 1 && !mbar_wait_warp(stage_free, (it - 1) & 1, abort_flag, p.status)) break;
       if (!mbar_wait_warp(dp_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
       {
@@ -529,7 +538,7 @@ cudaError_t launch_bwd_tc_t(const BwdMaps& maps, const BwdParams& p, cudaStream_
   if (e != cudaSuccess) return e;
   if (fa.numRegs != static_cast<int>(L::kLaunchRegs)) return cudaErrorInvalidConfiguration;
   const dim3 grid(p.cu_seqlens ? p.nseq * p.Hkv : p.B * p.Hkv, p.n_ktiles);
-  kern<<<grid, L::kThreads, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, maps.dout, p);
+  kern<<<grid, L::kThreads, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, maps.dout, maps.dq_acc, p);
   return cudaGetLastError();
 }
 

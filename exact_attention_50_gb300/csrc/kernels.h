@@ -67,9 +67,10 @@ struct BwdParams {
 };
 
 // Tensor maps for the tcgen05 backward: 3-D {d, rows, heads} with the layout's row / head
-// strides and a {64, 128, 1} box, for dense and varlen tensors alike.
+// strides and a {64, 128, 1} box, for dense and varlen tensors alike; and the fp32 dQ
+// accumulator as 2-D {d, rows} with a {32, 128} box (128-byte swizzle) for tile reductions.
 struct BwdMaps {
-  CUtensorMap q, k, v, dout;
+  CUtensorMap q, k, v, dout, dq_acc;
 };
 
 cudaError_t launch_bwd_preprocess(const BwdParams& p, attn_dtype_t dtype, bool zero_acc, cudaStream_t stream);
