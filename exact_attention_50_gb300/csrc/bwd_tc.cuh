@@ -45,14 +45,21 @@ struct BwdLayout {
   static constexpr int kOffdO = kOffQ + kQStages * kTileBytes;     // kQStages tiles
   static constexpr int kOffdSh = kOffdO + kQStages * kTileBytes;   // dS^T hi [128 keys x 128 queries]
   static constexpr int kOffdSl = kOffdSh + 2 * kChunkBytes;        // dS^T lo
-  static constexpr int kOffRow = kOffdSl + 2 * kChunkBytes;        // LSE*log2e and D, 2 buffers each
+  // dQ staging for the tile reductions: fp32 {32 columns, 128 rows} boxes of 16 KB.  Columns
+  // 0-63 have a buffer of their own; columns 64-127 (DP = 128) go through the dS lo area.
+  static constexpr int kOwnStageChunks = 2;
+  static constexpr int kLoStageChunks = DP / 32 - kOwnStageChunks;
+  static constexpr int kOffStage = kOffdSl + 2 * kChunkBytes;
+  static constexpr int kOffRow = kOffStage + kOwnStageChunks * kChunkBytes;  // LSE*log2e and D, 2 buffers each
   static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
   // kv_full, q_full[QS], q_empty[QS], do_full[QS], do_empty[QS], s_full, dp_full, p_full,
-  // dv_done, ds_full, stage_free, dq_full, dq_free, dkdv_done, rows_ready, stage_full, drain
-  static constexpr int kNumBars = 1 + 4 * kQStages + 12;
+  // dv_done, ds_full, dsl_free, stage_free, dq_full, dq_free, dkdv_done, rows_ready,
+  // stage_full, drain
+  static constexpr int kNumBars = 1 + 4 * kQStages + 13;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kBytes = kOffMisc + 16;
-  static constexpr int kSmemAlloc = kBytes + 1024;
+  static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
+  static_assert(kSmemAlloc <= 227 * 1024, "shared memory over the per-CTA limit");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 256 + DP;
   static constexpr uint32_t kColdQ = kColdP;
@@ -92,14 +99,21 @@ __global__ void __launch_bounds__(512, 1)
   constexpr int QS = L::kQStages;
   constexpr int kChunks = DP / 64;
   constexpr int kEw = L::kEwThreads;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The 128-byte swizzle atoms need 1024-byte aligned tiles and the layout has no slack to
+  // realign: refuse to run (before any barrier or allocation) if the base is not aligned.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) raise_status(p.status, ATTN_ERR_CUDA);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
   uint8_t* sQ = smem + L::kOffQ;
   uint8_t* sdO = smem + L::kOffdO;
   uint8_t* sdSh = smem + L::kOffdSh;
   uint8_t* sdSl = smem + L::kOffdSl;
+  uint8_t* sStage = smem + L::kOffStage;
   float* sLse = reinterpret_cast<float*>(smem + L::kOffRow);  // [2][128]
   float* sD = sLse + 256;                                       // [2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
@@ -113,8 +127,9 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* p_full = dp_full + 1;
   uint64_t* dv_done = p_full + 1;
   uint64_t* ds_full = dv_done + 1;
-  // the dS area is reused to stage dQ tiles: free once the tile's reduction has read it
-  uint64_t* stage_free = ds_full + 1;
+  // the dS lo area also stages dQ columns 64-127: free once the tile's reduction has read it
+  uint64_t* dsl_free = ds_full + 1;
+  uint64_t* stage_free = dsl_free + 1;  // the reductions have read the own staging buffer
   uint64_t* dq_full = stage_free + 1;
   uint64_t* dq_free = dq_full + 1;
   uint64_t* dkdv_done = dq_free + 1;
@@ -170,6 +185,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(p_full, kEw / 32);  // one arrival per warp
     mbar_init(dv_done, 1);
     mbar_init(ds_full, kEw / 32);
+    mbar_init(dsl_free, 1);
     mbar_init(stage_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);
@@ -332,17 +348,19 @@ __global__ void __launch_bounds__(512, 1)
     const int t = quad * 32 + lane;  // TMEM lane: query row of dQ, key row of dK / dV
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
-    // dQ_t goes from TMEM into the dS area of shared memory (free: the dK and dQ MMAs that read
-    // dS have completed when dq_full arrives), in the 128-byte swizzled layout of the
-    // accumulator map's {32, 128} box, chunk c of 32 columns at c * 16 KB; the TMEM columns are
-    // released at once, and one thread adds the staged tile into the fp32 accumulator with
-    // tile reductions.  Rows of the tile past the sequence hold exact zeros (P = 0 there), so
-    // they add nothing; rows past the accumulator are skipped by the map.
-    uint8_t* stage = sdSh;
+    // dQ_t goes from TMEM through shared memory into the fp32 accumulator by tile reductions,
+    // chunk c of 32 columns in the 128-byte swizzled layout of the accumulator map's {32, 128}
+    // box: chunks 0 and 1 in their own staging buffer, chunks 2 and 3 (DP = 128) in the dS lo
+    // area, free once the dK and dQ MMAs that read it have completed (dq_full).  The TMEM
+    // columns are released as soon as they are loaded, and the dS lo chunks are reduced first,
+    // so the elementwise warps may write the next dS lo as soon as they have been read.  Rows
+    // of the tile past the sequence hold exact zeros (P = 0 there), so they add nothing; rows
+    // past the accumulator are skipped by the map.
     for (int it = 0; it < n_it; ++it) {
       const int qt = qt0 + it % per_head;
       const int row0 = static_cast<int>(static_cast<size_t>(hq0 + it / per_head) * N + seq_start) + qt * kBM;
       if (!mbar_wait_warp(dq_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+      if (it >= 1 && !mbar_wait_warp(stage_free, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < DP / 32; ++c) {
@@ -354,7 +372,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_before();
           mbar_arrive_warp(dq_free);  // the dQ columns may be overwritten once everything is loaded
         }
-        uint8_t* row = stage + c * 16384 + t * 128;
+        uint8_t* row = (c < L::kOwnStageChunks ? sStage + c * 16384 : sdSl + (c - L::kOwnStageChunks) * 16384) + t * 128;
 #pragma unroll
         for (int g = 0; g < 8; ++g)
           *reinterpret_cast<uint4*>(row + ((g ^ (t & 7)) << 4)) = make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]);
@@ -364,12 +382,20 @@ __global__ void __launch_bounds__(512, 1)
       if (warp == 8 && lane == 0) {
         if (!mbar_wait(stage_full, it & 1, abort_flag, p.status)) { ok = false; }
         if (ok) {
-#pragma unroll
-          for (int c = 0; c < DP / 32; ++c)
-            if (c * 32 < p.d) tma_reduce_add_2d(&tmAcc, stage + c * 16384, c * 32, row0);
+          if (L::kLoStageChunks > 0) {
+            for (int c = L::kOwnStageChunks; c < DP / 32; ++c)
+              if (c * 32 < p.d) tma_reduce_add_2d(&tmAcc, sdSl + (c - L::kOwnStageChunks) * 16384, c * 32, row0);
+            bulk_commit();
+          }
+          for (int c = 0; c < L::kOwnStageChunks; ++c)
+            if (c * 32 < p.d) tma_reduce_add_2d(&tmAcc, sStage + c * 16384, c * 32, row0);
           bulk_commit();
-          bulk_wait_read();
-          mbar_arrive(stage_free);  // the dS area may take the next tile's dS
+          if (L::kLoStageChunks > 0) {
+            bulk_wait_read<1>();     // every group but the last: the dS lo chunks
+            mbar_arrive(dsl_free);   // the dS lo area may take the next tile's dS lo
+          }
+          bulk_wait_read<0>();
+          mbar_arrive(stage_free);
         }
       }
       __syncwarp();
@@ -483,8 +509,9 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_before();
       mbar_arrive_warp(p_full);
       load_rows(it + 1);  // prefetch the next tile's LSE and D
-      // ---- phase 2: dS^T = P^T (dP^T - D), hi/lo into shared memory
-      if (it >= 1 && !mbar_wait_warp(stage_free, (it - 1) & 1, abort_flag, p.status)) break;
+      // ---- phase 2: dS^T = P^T (dP^T - D), hi/lo into shared memory.  dp_full also means the
+      // previous tile's dK and dQ MMAs have completed (dP^T is issued after its dQ read-out), so
+      // the dS hi area is free; the dS lo area waits for the reductions of the dQ chunks staged in it.
       if (!mbar_wait_warp(dp_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
       {
@@ -501,17 +528,24 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
       tc_fence_before();  // the dP columns are consumed (the dQ MMA may overwrite them)
+      uint4 lo[8];
 #pragma unroll
       for (int gi = 0; gi < 8; ++gi) {
         const int gq = half * 8 + gi;  // 16-byte granule index over the 128 queries
         const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
-        uint4 a, c;
-        split_pack<T>(pv[gi * 8 + 0], pv[gi * 8 + 1], a.x, c.x);
-        split_pack<T>(pv[gi * 8 + 2], pv[gi * 8 + 3], a.y, c.y);
-        split_pack<T>(pv[gi * 8 + 4], pv[gi * 8 + 5], a.z, c.z);
-        split_pack<T>(pv[gi * 8 + 6], pv[gi * 8 + 7], a.w, c.w);
+        uint4 a;
+        split_pack<T>(pv[gi * 8 + 0], pv[gi * 8 + 1], a.x, lo[gi].x);
+        split_pack<T>(pv[gi * 8 + 2], pv[gi * 8 + 3], a.y, lo[gi].y);
+        split_pack<T>(pv[gi * 8 + 4], pv[gi * 8 + 5], a.z, lo[gi].z);
+        split_pack<T>(pv[gi * 8 + 6], pv[gi * 8 + 7], a.w, lo[gi].w);
         *reinterpret_cast<uint4*>(sdSh + off) = a;
-        *reinterpret_cast<uint4*>(sdSl + off) = c;
+      }
+      if (L::kLoStageChunks > 0 && it >= 1 && !mbar_wait_warp(dsl_free, (it - 1) & 1, abort_flag, p.status)) break;
+#pragma unroll
+      for (int gi = 0; gi < 8; ++gi) {
+        const int gq = half * 8 + gi;
+        const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
+        *reinterpret_cast<uint4*>(sdSl + off) = lo[gi];
       }
       fence_async_smem();
       mbar_arrive_warp(ds_full);
