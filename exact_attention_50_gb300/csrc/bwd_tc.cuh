@@ -454,15 +454,20 @@ __global__ void __launch_bounds__(512, 1)
     const int key = kt * kBN + t;
     const bool key_ok = key < seq_len;
     const float sl2 = p.scale_log2;
-    // row terms of tile `it`, loaded one tile ahead by threads 0..127
+    // The next tile's row terms are loaded one tile ahead and used only when they are written to
+    // shared memory at the start of that tile, so no thread waits for the loads in between.
+    // Rows past the sequence read its last row and are replaced there.
     float lse_next = 0.f, d_next = 0.f;
+    bool row_next = false;
     auto load_rows = [&](int it) {
       if (threadIdx.x < 128 && it < n_it) {
         const int qt = qt0 + it % per_head;
         const size_t row_base = static_cast<size_t>(hq0 + it / per_head) * N + seq_start;
         const int q = qt * kBM + threadIdx.x;
-        lse_next = q < seq_len ? p.lse[row_base + q] * 1.4426950408889634f : INFINITY;
-        d_next = q < seq_len ? p.delta[row_base + q] : 0.f;
+        row_next = q < seq_len;
+        const size_t r = row_base + (row_next ? q : seq_len - 1);
+        lse_next = p.lse[r];
+        d_next = p.delta[r];
       }
     };
     load_rows(0);
@@ -471,8 +476,8 @@ __global__ void __launch_bounds__(512, 1)
       float* lse_buf = sLse + (it & 1) * 128;
       float* d_buf = sD + (it & 1) * 128;
       if (threadIdx.x < 128) {
-        lse_buf[threadIdx.x] = lse_next;
-        d_buf[threadIdx.x] = d_next;
+        lse_buf[threadIdx.x] = row_next ? lse_next * 1.4426950408889634f : INFINITY;
+        d_buf[threadIdx.x] = row_next ? d_next : 0.f;
       }
       mbar_arrive_warp(rows_ready);
       if (!mbar_wait_warp(rows_ready, it & 1, abort_flag, p.status)) break;
