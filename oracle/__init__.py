@@ -6,7 +6,7 @@ nothing from the product package.
 
 Every function takes and returns float64 NumPy arrays in the layouts of the C source:
 dense Q/O/dO/dQ [B,Hq,N,d], K/V/dK/dV [B,Hkv,N,d], LSE [B,Hq,N]; varlen qkv [T,3,H,d],
-out [T,H,d], LSE [H,T].  ``scale=None`` means the default 1/sqrt(d).
+out [T,H,d], LSE [H,T]; KV cache q/o [B,Hq,Nq,d], k/v [B,Hkv,Nk,d], LSE [B,Hq,Nq].  ``scale=None`` means the default 1/sqrt(d).
 """
 from __future__ import annotations
 
@@ -57,6 +57,7 @@ def _bind(lib):
     lib.oracle_bwd_sampled.argtypes = ([_dp] * 4 + [_i64p, c_long, _dp, _i64p, c_long, _dp, _dp]
                                        + [c_int] * 6 + [c_double])
     lib.oracle_fwd_varlen.argtypes = [_dp, _i32p, c_int, c_int, _dp, _dp, c_int, c_int, c_int, c_double]
+    lib.oracle_fwd_kvcache.argtypes = [_dp, _dp, _dp, _i32p, _dp, _dp] + [c_int] * 7 + [c_double]
     lib.oracle_num_threads.restype = c_int
     lib.oracle_set_num_threads.argtypes = [c_int]
     return lib
@@ -192,3 +193,28 @@ def fwd_varlen(qkv, cu_seqlens, causal: bool, scale=None, lib=None):
     if rc:
         raise ValueError(f"oracle_fwd_varlen rejected its arguments ({rc})")
     return out, lse
+
+
+def fwd_kvcache(q, k, v, cache_seqlens, causal: bool, scale=None, lib=None):
+    """Returns (O [B,Hq,Nq,d], LSE [B,Hq,Nq]) for queries q against caches k, v [B,Hkv,Nk,d]
+    holding cache_seqlens[b] valid keys (None: all Nk); causal aligns the queries with the
+    last Nq cache positions.  Rows that see no key: O = 0, LSE = -inf."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if (Bk, dk) != (B, d) or v.shape != k.shape:
+        raise ValueError("q, k and v shapes disagree")
+    lens = None
+    if cache_seqlens is not None:
+        lens = np.ascontiguousarray(np.asarray(cache_seqlens, dtype=np.int32).reshape(-1))
+        if lens.shape[0] != B:
+            raise ValueError("cache_seqlens must have B entries")
+    o = np.empty((B, Hq, Nq, d))
+    lse = np.empty((B, Hq, Nq))
+    lib = lib or _load()
+    rc = lib.oracle_fwd_kvcache(_ptr(q), _ptr(k), _ptr(v),
+                                None if lens is None else lens.ctypes.data_as(_i32p),
+                                _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, int(causal), _scale(scale))
+    if rc:
+        raise ValueError(f"oracle_fwd_kvcache rejected its arguments ({rc})")
+    return o, lse

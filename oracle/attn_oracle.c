@@ -401,3 +401,65 @@ int oracle_fwd_varlen(const double *qkv, const int32_t *cu, int nseq, int T, dou
     }
     return err ? -2 : 0;
 }
+
+/* KV-cache (and cross-attention) forward: Nq queries against a cache of up to Nk keys per
+ * (batch, kv head) (FlashAttention-T review, 应用场景: blocked KV-cache computation for
+ * inference; the prefill / decode split of the same review).  q [B,Hq,Nq,d], k and v
+ * [B,Hkv,Nk,d], lens [B] (NULL: every cache holds Nk keys; else 0 <= lens[b] <= Nk),
+ * o [B,Hq,Nq,d], lse [B,Hq,Nq] (may be NULL).
+ *
+ * Query i of batch b sees the keys j < L = lens[b]; when causal, only j <= L - Nq + i: the
+ * queries are the last Nq positions of a sequence of L tokens (bottom-right alignment; with
+ * Nq == L it is the self-attention mask j <= i).  A row that sees no key has O = 0 and
+ * LSE = -inf (the empty sum).  Otherwise the row is the plain softmax over its visible keys,
+ * written out like the dense rows: explicit scores, max, sum, normalised weights. */
+int oracle_fwd_kvcache(const double *q, const double *k, const double *v, const int32_t *lens,
+                       double *o, double *lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                       int causal, double scale) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0 || Hq % Hkv != 0) return -1;
+    if (!(scale >= 0.0)) return -1;
+    if (lens)
+        for (int b = 0; b < B; ++b) if (lens[b] < 0 || lens[b] > Nk) return -1;
+    double sc = default_scale(scale, d);
+    int G = Hq / Hkv;
+    long rows = (long)B * Hq * Nq;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s_row = malloc(sizeof(double) * (Nk > 0 ? Nk : 1));
+        if (!s_row) err = 1;
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < rows; ++r) {
+            if (!s_row) continue;
+            int i = (int)(r % Nq), bh = (int)(r / Nq), b = bh / Hq, h = bh % Hq, kvh = h / G;
+            int L = lens ? lens[b] : Nk;
+            int last = causal ? L - Nq + i : L - 1; /* last visible key */
+            if (last > L - 1) last = L - 1;
+            const double *qi = q + ((long)bh * Nq + i) * d;
+            const double *kb = k + ((long)b * Hkv + kvh) * (long)Nk * d;
+            const double *vb = v + ((long)b * Hkv + kvh) * (long)Nk * d;
+            double *oi = o + r * d;
+            for (int c = 0; c < d; ++c) oi[c] = 0.0;
+            if (last < 0) {
+                if (lse) lse[r] = -INFINITY;
+                continue;
+            }
+            double m = -INFINITY;
+            for (int j = 0; j <= last; ++j) {
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += qi[c] * kb[(long)j * d + c];
+                s_row[j] = sc * acc;
+                if (s_row[j] > m) m = s_row[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j <= last; ++j) l += exp(s_row[j] - m);
+            for (int j = 0; j <= last; ++j) {
+                double pj = exp(s_row[j] - m) / l;
+                for (int c = 0; c < d; ++c) oi[c] += pj * vb[(long)j * d + c];
+            }
+            if (lse) lse[r] = m + log(l);
+        }
+        free(s_row);
+    }
+    return err ? -2 : 0;
+}

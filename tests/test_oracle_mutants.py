@@ -25,6 +25,13 @@ MUTANTS = [
     ("dQ uses V instead of K", "const double *kj = p->k + (long)j * p->kv_stride;\n                for",
      "const double *kj = p->v + (long)j * p->kv_stride;\n                for", None),
     ("varlen K read from the V slot", "p.k = qkv + (long)start * tok + 1L * H * d", "p.k = qkv + (long)start * tok + 2L * H * d", None),
+    ("kvcache causal mask top-left aligned", "int last = causal ? L - Nq + i : L - 1;",
+     "int last = causal ? i : L - 1;", None),
+    ("kvcache causal mask one key late", "int last = causal ? L - Nq + i : L - 1;",
+     "int last = causal ? L - Nq + i + 1 : L - 1;", None),
+    ("kvcache ignores the cache length", "int L = lens ? lens[b] : Nk;", "int L = Nk;", None),
+    ("kvcache GQA heads strided", "kvh = h / G;", "kvh = h % Hkv;", None),
+    ("kvcache empty row LSE 0", "if (lse) lse[r] = -INFINITY;", "if (lse) lse[r] = 0.0;", None),
     ("default scale is 1/d", "return scale == 0.0 ? 1.0 / sqrt((double)d) : scale;",
      "return scale == 0.0 ? 1.0 / (double)d : scale;", None),
 ]

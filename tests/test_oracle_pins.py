@@ -319,3 +319,110 @@ def test_flop_count_matches_page_example():
     ex = json.load(open(os.path.join(GOLDEN, "flop_count_example.json")))
     # the forward counts two such contractions per head: half of it is one contraction
     assert workloads.fwd_flops(1, 1, ex["N"], ex["d"], False) / 2 == ex["one_gemm_one_head_flops"]
+
+
+# ---------------------------------------------------------------- KV cache / cross-attention
+
+def _lower_right_counts(Nq, L, causal):
+    """Visible keys per query row, from torch's own bottom-right causal mask (a library
+    definition of the alignment, not the oracle's rule retyped)."""
+    if L == 0:
+        return np.zeros(Nq, dtype=np.int64)
+    if not causal:
+        return np.full(Nq, L, dtype=np.int64)
+    import warnings
+    from torch.nn.attention.bias import causal_lower_right
+    with warnings.catch_warnings():
+        warnings.simplefilter("ignore")
+        mask = causal_lower_right(Nq, L)._materialize(device="cpu")
+    return mask.sum(dim=-1).numpy().astype(np.int64)
+
+
+def _kv_inputs(seed, B=3, Hq=4, Hkv=2, Nq=5, Nk=11, d=16):
+    rng = np.random.default_rng(seed)
+    return rng, rand(rng, B, Hq, Nq, d), rand(rng, B, Hkv, Nk, d), rand(rng, B, Hkv, Nk, d)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kvcache_zero_queries_give_log_count(causal, lib=None):
+    """Q = 0 -> every visible score is 0 -> LSE_i = ln(visible keys) (-inf when none) and O_i
+    is the mean of the visible V rows (0 when none).  Lengths 11, 4 (< Nq: under the causal
+    mask the first row sees nothing) and 0 (an empty cache)."""
+    rng, q, k, v = _kv_inputs(31)
+    q[:] = 0.0
+    lens = [11, 4, 0]
+    B, Hq, Nq, d = q.shape
+    G = Hq // k.shape[1]
+    o, lse = oracle.fwd_kvcache(q, k, v, lens, causal, lib=lib)
+    for b, L in enumerate(lens):
+        cnt = _lower_right_counts(Nq, L, causal)
+        for h in range(Hq):
+            for i in range(Nq):
+                c = int(cnt[i])
+                if c == 0:
+                    assert lse[b, h, i] == -np.inf
+                    np.testing.assert_array_equal(o[b, h, i], 0.0)
+                else:
+                    np.testing.assert_allclose(lse[b, h, i], math.log(c), rtol=0, atol=1e-13)
+                    np.testing.assert_allclose(o[b, h, i], v[b, h // G, :c].mean(axis=0), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kvcache_matches_torch_lower_right_sdpa(causal, lib=None):
+    """torch's float64 SDPA per batch on the cache cut to its length, with the library's
+    bottom-right causal mask and GQA; rows that see no key are checked by the pin above."""
+    _, q, k, v = _kv_inputs(32, B=3, Hq=6, Hkv=3, Nq=7, Nk=20, d=16)
+    lens = [20, 9, 3]
+    sc = 0.3
+    o, lse = oracle.fwd_kvcache(q, k, v, lens, causal, scale=sc, lib=lib)
+    from torch.nn.attention.bias import causal_lower_right
+    import warnings
+    for b, L in enumerate(lens):
+        tq = torch.tensor(q[b:b + 1])
+        tk, tv = torch.tensor(k[b:b + 1, :, :L]), torch.tensor(v[b:b + 1, :, :L])
+        with warnings.catch_warnings():
+            warnings.simplefilter("ignore")
+            mask = causal_lower_right(q.shape[2], L) if causal else None
+            ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=sc, enable_gqa=True).numpy()
+        cnt = _lower_right_counts(q.shape[2], L, causal)
+        seen = cnt > 0
+        np.testing.assert_allclose(o[b][:, seen], ref[0][:, seen], rtol=0, atol=1e-12)
+        # LSE: torch.logsumexp of the scores of the visible keys
+        s = sc * torch.einsum("hid,hjd->hij", torch.tensor(q[b]), torch.tensor(np.repeat(k[b, :, :L], q.shape[1] // k.shape[1], axis=0)))
+        if causal:
+            with warnings.catch_warnings():
+                warnings.simplefilter("ignore")
+                vis = causal_lower_right(q.shape[2], L)._materialize(device="cpu")
+            s = s.masked_fill(~vis, float("-inf"))
+        np.testing.assert_allclose(lse[b][:, seen], torch.logsumexp(s, dim=-1).numpy()[:, seen], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kvcache_full_square_cache_is_self_attention(causal, lib=None):
+    """Nq == Nk with every cache full: the dense (self-attention) oracle, mask included."""
+    _, q, k, v = _kv_inputs(33, B=2, Hq=4, Hkv=2, Nq=9, Nk=9, d=16)
+    o, lse = oracle.fwd_kvcache(q, k, v, None, causal, lib=lib)
+    o2, lse2 = oracle.fwd(q, k, v, causal, lib=lib)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-14)
+
+
+def test_kvcache_ignores_cache_rows_past_length(lib=None):
+    """Cache rows at or past cache_seqlens[b] do not enter the result."""
+    rng, q, k, v = _kv_inputs(34)
+    lens = [6, 11, 1]
+    o, lse = oracle.fwd_kvcache(q, k, v, lens, True, lib=lib)
+    k2, v2 = k.copy(), v.copy()
+    for b, L in enumerate(lens):
+        k2[b, :, L:] = rand(rng, *k2[b, :, L:].shape) * 50
+        v2[b, :, L:] = rand(rng, *v2[b, :, L:].shape) * 50
+    o2, lse2 = oracle.fwd_kvcache(q, k2, v2, lens, True, lib=lib)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_kvcache_rejects_bad_lengths(lib=None):
+    _, q, k, v = _kv_inputs(35)
+    for lens in ([12, 1, 1], [-1, 2, 2]):
+        with pytest.raises(ValueError):
+            oracle.fwd_kvcache(q, k, v, lens, False, lib=lib)
