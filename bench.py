@@ -96,6 +96,8 @@ def read_peaks():
 
 def workload_flops(wl, lengths=None):
     from exact_attention_50_gb300 import workloads as W
+    if "Nq" in wl.extra:  # KV cache: forward only, over the keys each query sees
+        return W.kvcache_fwd_flops(lengths, wl.Hq, wl.extra["Nq"], wl.d, wl.causal), 0.0
     if wl.varlen:
         f = W.varlen_fwd_flops(lengths, wl.Hq, wl.d, wl.causal)
         return f, (2.5 * f if wl.backward else 0.0)
@@ -179,6 +181,26 @@ def committed_traffic(kernel: str, workload: str):
 
 # ------------------------------------------------------------------ CPU oracle timing
 
+def kv_oracle_sample(wl, seconds: float, seed: int = 0):
+    """The oracle's KV-cache forward over whole batches of the decode workload (all heads, the
+    batch's cache) until `seconds` have passed.  Returns (TFLOP/s, description)."""
+    import oracle
+    from exact_attention_50_gb300 import workloads as W
+    Nq = wl.extra["Nq"]
+    q, k, v, cl = W.kvcache_inputs(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, wl.dtype, wl.extra["lens"], seed=seed)
+    t0, flops, done = time.perf_counter(), 0.0, 0
+    for b in range(wl.B):
+        L = int(cl[b])
+        oracle.fwd_kvcache(q[b:b + 1].double().numpy(), k[b:b + 1, :, :L].double().numpy(),
+                           v[b:b + 1, :, :L].double().numpy(), [L], wl.causal, wl.scale)
+        flops += W.kvcache_fwd_flops([L], wl.Hq, Nq, wl.d, wl.causal)
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, f"{done} of {wl.B} batches (all {wl.Hq} heads, their whole cache), fwd, fp64"
+
+
 def oracle_sample(wl, seconds: float, seed: int = 0):
     """Times the fp64 oracle on a bounded sample of the workload: whole kv groups (all query
     heads of one kv head, one batch) forward + backward, until `seconds` have passed.  Returns
@@ -190,6 +212,9 @@ def oracle_sample(wl, seconds: float, seed: int = 0):
     oracle.build()
     oracle.set_num_threads(os.cpu_count() or 1)
     cores = oracle.num_threads()
+    if "Nq" in wl.extra:
+        v_, sample = kv_oracle_sample(wl, seconds, seed)
+        return v_, cores, sample
     if wl.varlen:
         qkv, cu, lengths, _ = W.varlen_inputs(wl.varlen, wl.Hq, wl.d, wl.dtype, seed=seed)
         done, flops, t0 = 0, 0.0, time.perf_counter()
@@ -260,7 +285,35 @@ def run_ours(args, rank, world, local):
     scale = 0.0 if wl.scale is None else float(wl.scale)
 
     lengths = None
-    if wl.varlen:
+    kv_bytes = None
+    if "Nq" in wl.extra:
+        Nq = wl.extra["Nq"]
+        q_h, k_h, v_h, cl_h = W.kvcache_inputs(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, wl.dtype, wl.extra["lens"],
+                                               seed=0)
+        lengths = cl_h.tolist()
+        q, k, v, cl = q_h.to(dev), k_h.to(dev), v_h.to(dev), cl_h.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(wl.B, wl.Hq, Nq, dtype=torch.float32, device=dev)
+        nsplit = lib.attn_fwd_kvcache_splits(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, 0)
+        nbytes = lib.attn_fwd_kvcache_workspace_bytes(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, 0)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        # a step serves one new token per sequence: its query in, its output out; the caches
+        # stay resident (in the end-to-end leg too: they are the state a decoder keeps)
+        host_in = [q_h]
+        dev_in = [q]
+        dev_out = [o]
+        # algorithmic HBM bytes: the K and V rows of each (batch, kv head) that its queries see,
+        # read once, plus Q read and O and LSE written (the split partials are not counted)
+        rows = wl.B * wl.Hq * Nq
+        kv_bytes = (sum(lengths) * wl.Hkv * wl.d * 2 * q_h.element_size() + 2 * rows * wl.d * q_h.element_size()
+                    + rows * 4)
+
+        def fwd_call():
+            return lib.attn_fwd_kvcache(q.data_ptr(), k.data_ptr(), v.data_ptr(), cl.data_ptr(), o.data_ptr(),
+                                        lse.data_ptr(), ws.data_ptr(), nbytes, wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d,
+                                        int(wl.causal), scale, 0, dt_code, 0, sp)
+        bwd_calls = []
+    elif wl.varlen:
         qkv_h, cu_h, lengths, _ = W.varlen_inputs(wl.varlen, wl.Hq, wl.d, wl.dtype, seed=0)
         T = qkv_h.shape[0]
         qkv = qkv_h.to(dev)
@@ -325,6 +378,7 @@ def run_ours(args, rank, world, local):
             ]
     calls = [fwd_call] + bwd_calls
     launches_per_step = len(calls)
+    kernels_per_step = launches_per_step + (1 if kv_bytes is not None else 0)  # + the split combine
     fwd_f, bwd_f = workload_flops(wl, lengths)
     step_flops = fwd_f + bwd_f
 
@@ -430,6 +484,15 @@ def run_ours(args, rank, world, local):
                 "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4) if peak else None,
                 "traffic": traffic, "peak_source": f"{peaks['source']} bf16 dense, sustained"}
+    if kv_bytes is not None:
+        # decode streams the caches once: HBM-bound; the call's time covers the forward kernel
+        # and the split combine
+        gbs = kv_bytes / (per_call_ms[0] * 1e-3) / 1e9
+        hbm = peaks.get("hbm_gbs")
+        roofline = {"kernel": "fwd_tc_kernel + kv_combine_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                    "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4) if hbm else None,
+                    "traffic": committed_traffic("fwd_tc_kernel", args.workload),
+                    "algorithmic_bytes": int(kv_bytes), "peak_source": f"{peaks['source']} HBM copy"}
     fwd_ms = per_call_ms[0]
     detail = {"fwd_ms": fwd_ms, "fwd_tflops": fwd_f / (fwd_ms * 1e-3) / 1e12,
               "fwd_frac": (fwd_f / (fwd_ms * 1e-3) / 1e12) / peak if peak else None}
@@ -453,12 +516,16 @@ def run_ours(args, rank, world, local):
                "step": "fwd + bwd (prepare, main, finish)" if bwd_calls else "fwd"}
         if wl.varlen:
             cfg["total_tokens"] = sum(lengths)
+        if kv_bytes is not None:
+            cfg.update({"queries_per_sequence": wl.extra["Nq"], "cache_capacity": wl.N,
+                        "cache_tokens": sum(lengths), "num_splits": nsplit,
+                        "step": "one decode forward (forward kernel + split combine)"})
         line = {"metric": "attention TFLOP/s (fwd+bwd)" if bwd_calls else "attention TFLOP/s (fwd)",
                 "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
                 "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,1))",
                 "config": cfg, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-                "gpu_launches": launches_per_step * K, "detail": detail}
+                "gpu_launches": kernels_per_step * K, "detail": detail}
     return line
 
 
@@ -477,7 +544,18 @@ def run_reference(args, rank, world):
     cores = oracle.num_threads()
     # one step = the oracle's fwd (+bwd) of one query head over its kv head (a slice of the
     # workload), rows sampled when a whole head would take too long
-    if wl.varlen:
+    if "Nq" in wl.extra:
+        Nq = wl.extra["Nq"]
+        q, k, v, cl = W.kvcache_inputs(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, wl.dtype, wl.extra["lens"], seed=0)
+        L = int(cl.min())  # the shortest cache of the batch: one batch per step
+        b = int(cl.argmin())
+        qn, kn, vn = q[b:b + 1].double().numpy(), k[b:b + 1, :, :L].double().numpy(), v[b:b + 1, :, :L].double().numpy()
+
+        def step():
+            oracle.fwd_kvcache(qn, kn, vn, [L], wl.causal, wl.scale)
+            return W.kvcache_fwd_flops([L], wl.Hq, Nq, wl.d, wl.causal)
+        sample = f"batch {b} (all {wl.Hq} heads, cache of {L} keys) per step, fwd, fp64"
+    elif wl.varlen:
         qkv, cu, lengths, _ = W.varlen_inputs(wl.varlen, wl.Hq, wl.d, wl.dtype, seed=0)
         s = int(np.argmin(lengths))
         a, b = cu.tolist()[s], cu.tolist()[s + 1]

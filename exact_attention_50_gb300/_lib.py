@@ -60,6 +60,12 @@ def load() -> ctypes.CDLL:
         lib.attn_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, i, i, i, vp, vp, ctypes.c_size_t, i, i, i, f, i, u, vp]
         lib.attn_bwd_varlen.restype = i
+        lib.attn_fwd_kvcache_splits.argtypes = [i, i, i, i, i, i]
+        lib.attn_fwd_kvcache_splits.restype = i
+        lib.attn_fwd_kvcache_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        lib.attn_fwd_kvcache_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_fwd_kvcache.argtypes = [vp] * 7 + [ctypes.c_size_t] + [i] * 7 + [f, i, i, u, vp]
+        lib.attn_fwd_kvcache.restype = i
         lib.attn_get_device_status.argtypes = [vp]
         lib.attn_get_device_status.restype = i
         lib.attn_status_string.argtypes = [i]
@@ -86,6 +92,20 @@ def attn_fwd_varlen(qkv, cu_seqlens, nseq, total_tokens, max_seqlen, out, lse, H
                     flags, stream) -> int:
     return load().attn_fwd_varlen(qkv, cu_seqlens, nseq, total_tokens, max_seqlen, out, lse, H, d, int(causal),
                                   float(scale), dtype, flags, stream)
+
+
+def attn_fwd_kvcache_splits(B, Hq, Hkv, Nq, Nk, num_splits) -> int:
+    return load().attn_fwd_kvcache_splits(B, Hq, Hkv, Nq, Nk, num_splits)
+
+
+def attn_fwd_kvcache_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, num_splits) -> int:
+    return load().attn_fwd_kvcache_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, num_splits)
+
+
+def attn_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, o, lse, workspace, workspace_bytes, B, Hq, Hkv, Nq, Nk, d,
+                     causal, scale, num_splits, dtype, flags, stream) -> int:
+    return load().attn_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, o, lse, workspace, workspace_bytes, B, Hq, Hkv,
+                                   Nq, Nk, d, int(causal), float(scale), int(num_splits), dtype, flags, stream)
 
 
 def attn_bwd_workspace_bytes(B, Hq, N, d) -> int:

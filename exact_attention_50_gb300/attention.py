@@ -145,6 +145,46 @@ def bwd_varlen(qkv, out, lse, dout, cu_seqlens, max_seqlen: int, causal: bool, s
     return dqkv
 
 
+def kvcache_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    """Bytes of the device workspace fwd_kvcache needs for these sizes and num_splits."""
+    return _lib.attn_fwd_kvcache_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, num_splits)
+
+
+def fwd_kvcache(q, k_cache, v_cache, cache_seqlens=None, causal: bool = False, scale=None, num_splits: int = 0,
+                out_f32: bool = False, with_lse: bool = True, workspace=None):
+    """KV-cache / cross-attention forward.  q [B,Hq,Nq,d]; k_cache, v_cache [B,Hkv,Nk,d];
+    cache_seqlens int32 [B] on the device (None: Nk keys each).  causal aligns the queries with
+    the last Nq keys of each cache.  num_splits: key ranges per (batch, kv head), 0 = chosen
+    from the sizes.  Returns (o [B,Hq,Nq,d], lse [B,Hq,Nq] or None)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n, q.dtype)
+    if q.dim() != 4 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("q must be [B,Hq,Nq,d] and k_cache, v_cache [B,Hkv,Nk,d]")
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, dk = k_cache.shape
+    if k_cache.shape[0] != B or dk != d:
+        raise ValueError("q and the caches disagree on batch or head_dim")
+    lens_ptr = None
+    if cache_seqlens is not None:
+        _require(cache_seqlens, "cache_seqlens", torch.int32)
+        if cache_seqlens.shape != (B,) or cache_seqlens.device != q.device:
+            raise ValueError("cache_seqlens must be int32 [B] on q's device")
+        lens_ptr = cache_seqlens.data_ptr()
+    o = torch.empty(q.shape, dtype=torch.float32 if out_f32 else q.dtype, device=q.device)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device) if with_lse else None
+    need = _lib.attn_fwd_kvcache_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, num_splits) if B * Nq > 0 else 0
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    elif workspace.numel() < need:
+        raise ValueError(f"workspace too small: {workspace.numel()} < {need} bytes")
+    st = _lib.attn_fwd_kvcache(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), lens_ptr, o.data_ptr(),
+                               lse.data_ptr() if lse is not None else None, workspace.data_ptr(), workspace.numel(),
+                               B, Hq, Hkv, Nq, Nk, d, causal, _scale_arg(scale), num_splits, _dtype_code(q),
+                               _lib.ATTN_FLAG_OUT_F32 if out_f32 else 0, _stream())
+    _lib._check(st, "attn_fwd_kvcache")
+    return o, lse
+
+
 class _AttnFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, causal, scale):

@@ -2,6 +2,7 @@
 // the per-device status word and dispatch to the kernels.  Nothing here allocates device
 // memory; every launch goes on the caller's stream.
 #include <cudaTypedefs.h>
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <initializer_list>
@@ -149,12 +150,12 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.scale_log2 = p.scale * kLog2e;
   p.out_f32 = (flags & ATTN_FLAG_OUT_F32) ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (f32) return from_cuda(attn::launch_fwd_f32(q, k, v, p, causal != 0, false, s));
+  if (f32) return from_cuda(attn::launch_fwd_f32(q, k, v, p, causal != 0, attn::kModeDense, s));
   FwdMaps maps;
   if (!make_dense_map(&maps.q, q, dtype, B * Hq, N, d) || !make_dense_map(&maps.k, k, dtype, B * Hkv, N, d) ||
       !make_dense_map(&maps.v, v, dtype, B * Hkv, N, d))
     return ATTN_ERR_CUDA;
-  return from_cuda(attn::launch_fwd_tc(maps, p, dtype, causal != 0, false, s));
+  return from_cuda(attn::launch_fwd_tc(maps, p, dtype, causal != 0, attn::kModeDense, s));
 }
 
 attn_status_t attn_fwd_varlen(const void* qkv, const int32_t* cu_seqlens, int nseq, int total_tokens,
@@ -191,13 +192,13 @@ attn_status_t attn_fwd_varlen(const void* qkv, const int32_t* cu_seqlens, int ns
   const size_t plane = static_cast<size_t>(H) * d;
   if (f32) {
     const float* base = static_cast<const float*>(qkv);
-    return from_cuda(attn::launch_fwd_f32(base, base + plane, base + 2 * plane, p, causal != 0, true, s));
+    return from_cuda(attn::launch_fwd_f32(base, base + plane, base + 2 * plane, p, causal != 0, attn::kModeVarlen, s));
   }
   FwdMaps maps;
   if (!make_packed_map(&maps.q, qkv, dtype, total_tokens, H, d)) return ATTN_ERR_CUDA;
   maps.k = maps.q;
   maps.v = maps.q;
-  return from_cuda(attn::launch_fwd_tc(maps, p, dtype, causal != 0, true, s));
+  return from_cuda(attn::launch_fwd_tc(maps, p, dtype, causal != 0, attn::kModeVarlen, s));
 }
 
 size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int d) {
@@ -364,6 +365,103 @@ attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout
   e = attn::launch_bwd_tc(maps, p, dtype, causal != 0, s);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_bwd_postprocess(p, dtype, s));
+}
+
+namespace {
+// Key ranges of the KV-cache forward: the requested count (0: enough work items for about
+// eight per SM of a 152-SM GPU), at most one per 128-key tile and at most 128; ranges are
+// whole tiles, and trailing empty ranges are dropped.
+struct KvSplit {
+  int n_splits, tiles_per_split;
+};
+KvSplit kv_split(int B, int Hq, int Hkv, int Nq, int Nk, int num_splits) {
+  const long tiles = (static_cast<long>(Nk) + attn::kBN - 1) / attn::kBN;
+  if (tiles <= 0) return {1, 1};
+  long want = num_splits;
+  if (want <= 0) {
+    const long rb = (static_cast<long>(Hq / Hkv) * Nq + attn::kBM - 1) / attn::kBM;
+    const long base = static_cast<long>(B) * Hkv * rb;
+    want = (8L * 152 + base - 1) / base;
+  }
+  want = std::min(want, std::min(tiles, 128L));
+  if (want < 1) want = 1;
+  const long tps = (tiles + want - 1) / want;
+  return {static_cast<int>((tiles + tps - 1) / tps), static_cast<int>(tps)};
+}
+}  // namespace
+
+int attn_fwd_kvcache_splits(int B, int Hq, int Hkv, int Nq, int Nk, int num_splits) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Nq <= 0 || Nk < 0 || num_splits < 0) return 0;
+  return kv_split(B, Hq, Hkv, Nq, Nk, num_splits).n_splits;
+}
+
+size_t attn_fwd_kvcache_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits) {
+  const int n = attn_fwd_kvcache_splits(B, Hq, Hkv, Nq, Nk, num_splits);
+  if (n <= 0 || d <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * Nq;
+  return round256(static_cast<size_t>(n) * rows * d * sizeof(float)) + round256(static_cast<size_t>(n) * rows * sizeof(float));
+}
+
+attn_status_t attn_fwd_kvcache(const void* q, const void* k_cache, const void* v_cache, const int32_t* cache_seqlens,
+                               void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                               int Nq, int Nk, int d, int causal, float scale, int num_splits, attn_dtype_t dtype,
+                               unsigned flags, void* stream) {
+  attn_status_t st = check_common(d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (B < 0 || Nq < 0 || Nk < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAG_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Nq == 0) return ATTN_OK;
+  // an empty cache (Nk == 0) is never read: its pointers may be null
+  if (!q || !o || (Nk > 0 && (!k_cache || !v_cache)) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(o, 16) || !aligned(lse, 4) || !aligned(cache_seqlens, 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < attn_fwd_kvcache_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, num_splits))
+    return ATTN_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  const long long R = static_cast<long long>(G) * Nq;
+  const long long bh = static_cast<long long>(B) * Hkv;
+  if (R > 0x7fffffffLL || bh * R > 0x7fffffffLL || static_cast<long long>(B) * Hq > 0x7fffffffLL)
+    return ATTN_ERR_UNSUPPORTED;
+  const KvSplit sp = kv_split(B, Hq, Hkv, Nq, Nk, num_splits);
+  const bool f32 = dtype == ATTN_F32;
+  const long long n_rb = (R + attn::kBM - 1) / attn::kBM;
+  if (f32 ? (Nq + 31) / 32 > 65535 : n_rb * bh * sp.n_splits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  const size_t rows = static_cast<size_t>(B) * Hq * Nq;
+
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.status = status_word();
+  if (!p.status) return ATTN_ERR_CUDA;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = Nk; p.d = d; p.G = G;
+  p.Nq = Nq; p.Nk = Nk; p.R = static_cast<int>(R);
+  p.cache_seqlens = cache_seqlens;
+  p.n_splits = sp.n_splits;
+  p.tiles_per_split = sp.tiles_per_split;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        round256(static_cast<size_t>(sp.n_splits) * rows * d * sizeof(float)));
+  p.n_qtiles = static_cast<int>(n_rb);
+  p.scale = resolve_scale(scale, d);
+  p.scale_log2 = p.scale * kLog2e;
+  p.out_f32 = (flags & ATTN_FLAG_OUT_F32) ? 1 : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Nk > 0) {  // an empty cache: no key for any row, the combine writes O = 0, LSE = -inf
+    cudaError_t e;
+    if (f32) {
+      e = attn::launch_fwd_f32(q, k_cache, v_cache, p, causal != 0, attn::kModeKv, s);
+    } else {
+      FwdMaps maps;
+      if (!make_dense_map(&maps.q, q, dtype, static_cast<int>(bh), static_cast<int>(R), d) ||
+          !make_dense_map(&maps.k, k_cache, dtype, static_cast<int>(bh), Nk, d) ||
+          !make_dense_map(&maps.v, v_cache, dtype, static_cast<int>(bh), Nk, d))
+        return ATTN_ERR_CUDA;
+      e = attn::launch_fwd_tc(maps, p, dtype, causal != 0, attn::kModeKv, s);
+    }
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return from_cuda(attn::launch_kv_combine(p, dtype, causal != 0, s));
 }
 
 attn_status_t attn_get_device_status(void* stream) {

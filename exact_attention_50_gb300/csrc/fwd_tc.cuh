@@ -94,15 +94,48 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>(a + ((1024u - (s & 1023u)) & 1023u));
 }
 
-// One work item: a 128-row query tile of one (batch, head) or (sequence, head).
+// One work item: a 128-row query tile of one (batch, head) or (sequence, head), or for a KV
+// cache a 128-row block of one (batch, kv head)'s R = G * Nq query rows against one range of
+// key tiles [j0, j0 + n_kv) (h is then the kv head and seq_len the cache length).
 struct FwdItem {
-  int b, h, qt, seq_start, seq_len, n_kv;
+  int b, h, qt, seq_start, seq_len, n_kv, j0, split;
   bool valid;
 };
 
-template <bool CAUSAL, bool VARLEN>
+template <bool CAUSAL, int MODE>
 __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int idx) {
+  constexpr bool VARLEN = MODE == kModeVarlen;
   FwdItem it;
+  it.j0 = 0;
+  it.split = 0;
+  if constexpr (MODE == kModeKv) {
+    // later row blocks first (under the causal mask they see the most keys), then (batch,
+    // kv head), then the key range
+    const int per_rb = p.B * p.Hkv * p.n_splits;
+    it.qt = p.n_qtiles - 1 - idx / per_rb;
+    const int rem = idx % per_rb;
+    const int bh = rem / p.n_splits;
+    it.split = rem % p.n_splits;
+    it.b = bh / p.Hkv;
+    it.h = bh % p.Hkv;
+    it.seq_start = 0;
+    it.valid = true;
+    int L = p.Nk;
+    if (p.cache_seqlens) {
+      L = p.cache_seqlens[it.b];
+      if (L < 0 || L > p.Nk) {
+        if (it.qt == 0 && it.h == 0 && it.split == 0) raise_status(p.status, ATTN_ERR_DEVICE_INPUT);
+        it.valid = false;
+        L = 0;
+      }
+    }
+    it.seq_len = L;
+    const int need_tiles = (kv_needed_keys(L, p.Nq, p.R, it.qt, CAUSAL) + kBN - 1) / kBN;
+    it.j0 = it.split * p.tiles_per_split;
+    it.n_kv = min(p.tiles_per_split, need_tiles - it.j0);
+    if (it.n_kv <= 0) it.valid = false;
+    return it;
+  }
   const int heads = VARLEN ? p.Hq : p.B * p.Hq;
   const int per_tile = VARLEN ? heads * p.nseq : heads;
   it.qt = p.n_qtiles - 1 - idx / per_tile;  // heaviest first
@@ -136,7 +169,7 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int idx) {
 
 // Walks the key tiles of a CTA's work items in order (item by item, key tile by key tile).
 // The producer and the MMA issuer each run such walks for their streams (Q/K, V; S, PV).
-template <bool CAUSAL, bool VARLEN>
+template <bool CAUSAL, int MODE>
 struct TileCursor {
   int idx, j;   // work item index and key tile within it
   uint32_t t;   // key tiles passed so far: ring position and barrier phases, across items
@@ -145,7 +178,7 @@ struct TileCursor {
   bool done;
   __device__ __forceinline__ void seek(const FwdParams& p, int n_items) {
     for (; idx < n_items; idx += gridDim.x) {
-      it = fwd_item<CAUSAL, VARLEN>(p, idx);
+      it = fwd_item<CAUSAL, MODE>(p, idx);
       if (it.valid) return;
     }
     done = true;
@@ -168,10 +201,12 @@ struct TileCursor {
   }
 };
 
-template <typename T, int DP, bool CAUSAL, bool VARLEN>
+template <typename T, int DP, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(320, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p, int n_items) {
+  constexpr bool VARLEN = MODE == kModeVarlen;
+  constexpr bool KV = MODE == kModeKv;
   using L = FwdLayout<DP>;
   constexpr int SQ = L::kStagesQ, SK = L::kStagesK, SV = L::kStagesV;
   constexpr int kChunks = DP / 64;
@@ -249,7 +284,7 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      TileCursor<CAUSAL, VARLEN> ck, cv;
+      TileCursor<CAUSAL, MODE> ck, cv;
       ck.start(p, n_items);
       cv.start(p, n_items);
       uint32_t nq = 0;      // Q tiles issued (one per item, slot item % 2)
@@ -266,6 +301,8 @@ __global__ void __launch_bounds__(320, 1)
             uint8_t* dst = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
             if constexpr (VARLEN)
               tma_load_4d(dst, &tmQ, q_full + qs, c * 64, it.h, 0, it.seq_start + it.qt * kBM);
+            else if constexpr (KV)
+              tma_load_3d(dst, &tmQ, q_full + qs, c * 64, it.qt * kBM, it.b * p.Hkv + it.h);
             else
               tma_load_3d(dst, &tmQ, q_full + qs, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
           }
@@ -282,6 +319,8 @@ __global__ void __launch_bounds__(320, 1)
               uint8_t* dst = sK + st * L::kTileBytes + c * L::kChunkBytes;
               if constexpr (VARLEN)
                 tma_load_4d(dst, &tmK, k_full + st, c * 64, it.h, 1, it.seq_start + ck.j * kBN);
+              else if constexpr (KV)
+                tma_load_3d(dst, &tmK, k_full + st, c * 64, (it.j0 + ck.j) * kBN, it.b * p.Hkv + it.h);
               else
                 tma_load_3d(dst, &tmK, k_full + st, c * 64, ck.j * kBN, it.b * p.Hkv + it.h / p.G);
             }
@@ -299,6 +338,8 @@ __global__ void __launch_bounds__(320, 1)
               uint8_t* dst = sV + st * L::kTileBytes + c * L::kChunkBytes;
               if constexpr (VARLEN)
                 tma_load_4d(dst, &tmV, v_full + st, c * 64, it.h, 2, it.seq_start + cv.j * kBN);
+              else if constexpr (KV)
+                tma_load_3d(dst, &tmV, v_full + st, c * 64, (it.j0 + cv.j) * kBN, it.b * p.Hkv + it.h);
               else
                 tma_load_3d(dst, &tmV, v_full + st, c * 64, cv.j * kBN, it.b * p.Hkv + it.h / p.G);
             }
@@ -381,7 +422,7 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
       uint32_t ic = 0;
       for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
-        const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
+        const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
         if (!it.valid) continue;
         const int n = it.n_kv;
         const uint32_t t0 = kv;
@@ -454,9 +495,16 @@ __global__ void __launch_bounds__(320, 1)
       return true;
     };
     for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
-      const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, idx);
+      const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
       if (!it.valid) continue;
-      const int q_row = it.qt * kBM + row;  // relative to the sequence
+      const int q_row = it.qt * kBM + row;  // relative to the sequence (KV cache: to the R rows)
+      // the last key this row sees: the diagonal under the causal mask, the sequence's end;
+      // for a KV cache row (query q_row % Nq) the same, aligned to the cache's last Nq keys
+      int last_key;
+      if constexpr (KV)
+        last_key = CAUSAL ? min(q_row % p.Nq + it.seq_len - p.Nq, it.seq_len - 1) : it.seq_len - 1;
+      else
+        last_key = CAUSAL ? min(q_row, it.seq_len - 1) : it.seq_len - 1;
       float m = -INFINITY, l = 0.f;          // l: this group's partial row sum
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t t = kv + j;
@@ -481,8 +529,8 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         mbar_arrive_warp(s_free + b);  // S buffer b may take S(t+2)
         // keys key0 + c with c > lim are masked (past the diagonal, or past the sequence)
-        const int key0 = j * kBN + grp * 64;
-        const int lim = CAUSAL ? min(q_row, it.seq_len - 1) - key0 : it.seq_len - 1 - key0;
+        const int key0 = (it.j0 + j) * kBN + grp * 64;
+        const int lim = last_key - key0;
         if (lim < 63) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) s[c] = c > lim ? -INFINITY : s[c];
@@ -583,13 +631,19 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t tl_last = kv - 1;
       if (!mbar_wait_warp(pv_done + (tl_last & 1), (tl_last >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      const bool valid = q_row < it.seq_len;
+      const bool valid = q_row < (KV ? p.R : it.seq_len);
       const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
       size_t row_off;
+      // a KV cache range writes its partial output in fp32 to its slice of the split buffer
+      const size_t kv_row = KV ? (static_cast<size_t>(it.split) * p.B * p.Hkv + static_cast<size_t>(it.b) * p.Hkv + it.h) * p.R + q_row : 0;
       if constexpr (VARLEN)
         row_off = (static_cast<size_t>(it.seq_start + q_row) * p.Hq + it.h) * p.d;
+      else if constexpr (KV)
+        row_off = kv_row * p.d;
       else
         row_off = ((static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row) * p.d;
+      const bool o_f32 = KV || p.out_f32;
+      void* const o_base = KV ? static_cast<void*>(p.o_part) : p.o;
       uint32_t r[32];
 #pragma unroll
       for (int c = 0; c < DP / 64; ++c) {
@@ -599,8 +653,8 @@ __global__ void __launch_bounds__(320, 1)
         const int col0 = grp * (DP / 2) + c * 32;
         if (valid && col0 < p.d) {
           const int ncol = min(32, p.d - col0);  // 16 or 32 (d is a multiple of 16)
-          if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + row_off + col0);
+          if (o_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o_base) + row_off + col0);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               if (i * 4 < ncol)
@@ -608,7 +662,7 @@ __global__ void __launch_bounds__(320, 1)
                                      __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
             }
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.o) + row_off + col0);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(o_base) + row_off + col0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               if (i * 8 < ncol) {
@@ -625,9 +679,11 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       mbar_arrive_warp(o_free);
-      if (grp == 0 && valid && p.lse) {
+      if (grp == 0 && valid && (KV || p.lse)) {
         const float lse = (m + __log2f(l_all)) * 0.69314718055994531f;
-        if constexpr (VARLEN)
+        if constexpr (KV)
+          p.lse_part[kv_row] = lse;
+        else if constexpr (VARLEN)
           p.lse[static_cast<size_t>(it.h) * p.total_tokens + it.seq_start + q_row] = lse;
         else
           p.lse[(static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row] = lse;
@@ -655,13 +711,15 @@ inline int sm_count() {
   return n;
 }
 
-template <typename T, int DP, bool CAUSAL, bool VARLEN>
+template <typename T, int DP, bool CAUSAL, int MODE>
 cudaError_t launch_fwd_tc_t(const FwdMaps& maps, const FwdParams& p, cudaStream_t stream) {
   using L = FwdLayout<DP>;
-  auto kern = fwd_tc_kernel<T, DP, CAUSAL, VARLEN>;
+  auto kern = fwd_tc_kernel<T, DP, CAUSAL, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  const long heads = VARLEN ? static_cast<long>(p.Hq) * p.nseq : static_cast<long>(p.B) * p.Hq;
+  const long heads = MODE == kModeVarlen ? static_cast<long>(p.Hq) * p.nseq
+                     : MODE == kModeKv   ? static_cast<long>(p.B) * p.Hkv * p.n_splits
+                                         : static_cast<long>(p.B) * p.Hq;
   const long items = heads * p.n_qtiles;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
@@ -669,20 +727,26 @@ cudaError_t launch_fwd_tc_t(const FwdMaps& maps, const FwdParams& p, cudaStream_
   return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t launch_fwd_tc_dtype(const FwdMaps& maps, const FwdParams& p, bool causal, bool varlen,
-                                cudaStream_t stream) {
-  const bool d64 = p.d <= 64;
-  if (d64) {
-    if (varlen) return causal ? launch_fwd_tc_t<T, 64, true, true>(maps, p, stream)
-                              : launch_fwd_tc_t<T, 64, false, true>(maps, p, stream);
-    return causal ? launch_fwd_tc_t<T, 64, true, false>(maps, p, stream)
-                  : launch_fwd_tc_t<T, 64, false, false>(maps, p, stream);
+template <typename T, int DP>
+cudaError_t launch_fwd_tc_dp(const FwdMaps& maps, const FwdParams& p, bool causal, int mode, cudaStream_t stream) {
+  switch (mode) {
+    case kModeVarlen:
+      return causal ? launch_fwd_tc_t<T, DP, true, kModeVarlen>(maps, p, stream)
+                    : launch_fwd_tc_t<T, DP, false, kModeVarlen>(maps, p, stream);
+    case kModeKv:
+      return causal ? launch_fwd_tc_t<T, DP, true, kModeKv>(maps, p, stream)
+                    : launch_fwd_tc_t<T, DP, false, kModeKv>(maps, p, stream);
+    default:
+      return causal ? launch_fwd_tc_t<T, DP, true, kModeDense>(maps, p, stream)
+                    : launch_fwd_tc_t<T, DP, false, kModeDense>(maps, p, stream);
   }
-  if (varlen) return causal ? launch_fwd_tc_t<T, 128, true, true>(maps, p, stream)
-                            : launch_fwd_tc_t<T, 128, false, true>(maps, p, stream);
-  return causal ? launch_fwd_tc_t<T, 128, true, false>(maps, p, stream)
-                : launch_fwd_tc_t<T, 128, false, false>(maps, p, stream);
+}
+
+template <typename T>
+cudaError_t launch_fwd_tc_dtype(const FwdMaps& maps, const FwdParams& p, bool causal, int mode,
+                                cudaStream_t stream) {
+  return p.d <= 64 ? launch_fwd_tc_dp<T, 64>(maps, p, causal, mode, stream)
+                   : launch_fwd_tc_dp<T, 128>(maps, p, causal, mode, stream);
 }
 
 }  // namespace attn

@@ -2,12 +2,12 @@
 #include "fwd_tc.cuh"
 
 namespace attn {
-cudaError_t launch_fwd_tc_bf16(const FwdMaps& maps, const FwdParams& p, bool causal, bool varlen,
+cudaError_t launch_fwd_tc_bf16(const FwdMaps& maps, const FwdParams& p, bool causal, int mode,
                                cudaStream_t stream);
 
-cudaError_t launch_fwd_tc(const FwdMaps& maps, const FwdParams& p, attn_dtype_t dtype, bool causal, bool varlen,
+cudaError_t launch_fwd_tc(const FwdMaps& maps, const FwdParams& p, attn_dtype_t dtype, bool causal, int mode,
                           cudaStream_t stream) {
-  if (dtype == ATTN_BF16) return launch_fwd_tc_bf16(maps, p, causal, varlen, stream);
-  return launch_fwd_tc_dtype<__half>(maps, p, causal, varlen, stream);
+  if (dtype == ATTN_BF16) return launch_fwd_tc_bf16(maps, p, causal, mode, stream);
+  return launch_fwd_tc_dtype<__half>(maps, p, causal, mode, stream);
 }
 }  // namespace attn

@@ -22,18 +22,48 @@ struct FwdParams {
   float scale;             // softmax scale (natural units)
   float scale_log2;        // scale * log2(e)
   int out_f32;             // write o as float32
+  // KV cache / cross-attention: q [B,Hq,Nq,d] read as [B*Hkv, R = G*Nq, d] (the G query heads
+  // of a kv head are consecutive), k and v [B,Hkv,Nk,d], cache_seqlens [B] (null: Nk each).
+  // The key tiles of a (batch, kv head) are cut into n_splits ranges of tiles_per_split tiles;
+  // each range writes its normalised fp32 partial output and LSE, combined afterwards.
+  int Nq, Nk, R;
+  const int32_t* cache_seqlens;
+  int n_splits, tiles_per_split;
+  float* o_part;           // [n_splits, B*Hkv*R, d]
+  float* lse_part;         // [n_splits, B*Hkv*R] (natural log)
 };
 
+// KV cache: the number of leading keys that some row of 128-row block rb of a (batch, kv head)
+// sees.  Row r of the block is query i = r % Nq; query i sees keys j < L, and when causal only
+// j <= L - Nq + i (the queries are the last Nq positions of an L-token sequence).  The
+// forward kernel and the split combine both derive the split ranges from it.
+__host__ __device__ inline int kv_needed_keys(int L, int Nq, int R, int rb, bool causal) {
+  if (!causal) return L;
+  const int r0 = rb * 128;
+  const int r1 = (r0 + 128 < R ? r0 + 128 : R) - 1;
+  const int max_i = (r0 / Nq == r1 / Nq) ? r1 % Nq : Nq - 1;
+  const int n = L - Nq + max_i + 1;
+  return n < 0 ? 0 : (n > L ? L : n);
+}
+
 // Tensor maps for the tcgen05 forward: Q, K, V (dense: 3-D {d, N, B*H}; varlen: the same
-// 4-D map {d, H, 3, T} three times).  Boxes are {64, 128(, 1)} with 128-byte swizzle.
+// 4-D map {d, H, 3, T} three times; KV cache: Q {d, R, B*Hkv}, K and V {d, Nk, B*Hkv}).
+// Boxes are {64, 128(, 1)} with 128-byte swizzle; rows past a map's extent load as zeros.
 struct FwdMaps {
   CUtensorMap q, k, v;
 };
 
-cudaError_t launch_fwd_tc(const FwdMaps& maps, const FwdParams& p, attn_dtype_t dtype, bool causal, bool varlen,
+// Work-item layouts of the forward kernels.
+constexpr int kModeDense = 0, kModeVarlen = 1, kModeKv = 2;
+
+cudaError_t launch_fwd_tc(const FwdMaps& maps, const FwdParams& p, attn_dtype_t dtype, bool causal, int mode,
                           cudaStream_t stream);
 cudaError_t launch_fwd_f32(const void* q, const void* k, const void* v, const FwdParams& p, bool causal,
-                           bool varlen, cudaStream_t stream);
+                           int mode, cudaStream_t stream);
+// KV cache: merges the n_splits partial outputs of every row into o (dtype, or fp32 when
+// out_f32 or dtype is fp32) and lse (nullable); a row with no visible key gets O = 0 and
+// LSE = -inf.
+cudaError_t launch_kv_combine(const FwdParams& p, attn_dtype_t dtype, bool causal, cudaStream_t stream);
 
 // Backward.
 struct BwdParams {

@@ -162,6 +162,106 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(const float* __restrict__ 
   }
 }
 
+// KV cache / cross-attention forward in fp32: CTA (batch * query head, 32-row query tile,
+// key range).  Query i of batch b sees the cache keys j < L = cache_seqlens[b] (Nk when
+// absent) and, when causal, only j <= L - Nq + i.  Range s covers the keys
+// [s * tiles_per_split * 128, (s + 1) * tiles_per_split * 128); every range writes its
+// normalised partial output and LSE (O = 0, LSE = -inf for a row that sees none of its keys),
+// which the split combine merges.
+template <bool CAUSAL>
+__global__ void __launch_bounds__(128) fwd_f32_kv_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                                                         const float* __restrict__ v, const FwdParams p) {
+  extern __shared__ float smem_f[];
+  const int dp1 = p.d + 1;
+  float* sK = smem_f;                  // [kTile][d+1]
+  float* sV = sK + kTile * dp1;        // [kTile][d]
+  float* sQ = sV + kTile * p.d;        // [kRows][d]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq, g = h / p.G;
+  const int qt = blockIdx.y, split = blockIdx.z;
+  const int d = p.d, Nq = p.Nq;
+  int L = p.Nk;
+  if (p.cache_seqlens) {
+    L = p.cache_seqlens[b];
+    if (L < 0 || L > p.Nk) {
+      if (threadIdx.x == 0 && h == 0 && qt == 0 && split == 0) raise_status(p.status, ATTN_ERR_DEVICE_INPUT);
+      L = 0;
+    }
+  }
+  const size_t qbase = (static_cast<size_t>(b) * p.Hq + h) * Nq * d;
+  const size_t kbase = (static_cast<size_t>(b) * p.Hkv + g) * p.Nk * d;
+  const int row0 = qt * kRows;
+  for (int idx = threadIdx.x; idx < kRows * d; idx += blockDim.x) {
+    const int r = idx / d, c = idx % d;
+    sQ[r * d + c] = (row0 + r < Nq) ? q[qbase + static_cast<size_t>(row0 + r) * d + c] : 0.f;
+  }
+  float m[8], l[8], acc[8][kColsPerLane];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kColsPerLane; ++i) acc[r][i] = 0.f;
+  }
+  const float sl2 = p.scale_log2;
+  const long span = static_cast<long>(p.tiles_per_split) * 128;
+  const int k_begin = static_cast<int>(min(static_cast<long>(L), split * span));
+  const int k_end = static_cast<int>(min(static_cast<long>(L), (split + 1) * span));
+  for (int key0 = k_begin; key0 < k_end; key0 += kTile) {
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < kTile * d; idx += blockDim.x) {
+      const int r = idx / d, c = idx % d;
+      const bool in = key0 + r < k_end;
+      sK[r * dp1 + c] = in ? k[kbase + static_cast<size_t>(key0 + r) * d + c] : 0.f;
+      sV[r * d + c] = in ? v[kbase + static_cast<size_t>(key0 + r) * d + c] : 0.f;
+    }
+    __syncthreads();
+    const int key = key0 + lane;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int lr = warp * 8 + r, qrow = row0 + lr;
+      float s = 0.f;
+      for (int c = 0; c < d; ++c) s = fmaf(sQ[lr * d + c], sK[lane * dp1 + c], s);
+      const bool masked = key >= k_end || (CAUSAL && key > L - Nq + qrow);
+      float x = masked ? -INFINITY : s * sl2;
+      float mx = x;
+      warp_max_sum(mx, true);
+      const float m_new = fmaxf(m[r], mx);
+      const float mb = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = exp2f(m[r] - mb);
+      const float pr = exp2f(x - mb);
+      float rs = pr;
+      warp_max_sum(rs, false);
+      l[r] = l[r] * alpha + rs;
+      m[r] = m_new;
+#pragma unroll
+      for (int i = 0; i < kColsPerLane; ++i) acc[r][i] *= alpha;
+      for (int jj = 0; jj < kTile; ++jj) {
+        const float pj = __shfl_sync(0xffffffffu, pr, jj);
+#pragma unroll
+        for (int i = 0; i < kColsPerLane; ++i) {
+          const int c = lane + 32 * i;
+          if (c < d) acc[r][i] = fmaf(pj, sV[jj * d + c], acc[r][i]);
+        }
+      }
+    }
+  }
+  const size_t rows = static_cast<size_t>(p.B) * p.Hq * Nq;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int qrow = row0 + warp * 8 + r;
+    if (qrow >= Nq) continue;
+    const size_t orow = static_cast<size_t>(split) * rows + (static_cast<size_t>(b) * p.Hq + h) * Nq + qrow;
+    const float inv_l = l[r] > 0.f ? 1.f / l[r] : 0.f;
+#pragma unroll
+    for (int i = 0; i < kColsPerLane; ++i) {
+      const int c = lane + 32 * i;
+      if (c < d) p.o_part[orow * d + c] = acc[r][i] * inv_l;
+    }
+    if (lane == 0) p.lse_part[orow] = l[r] > 0.f ? (m[r] + log2f(l[r])) / kLog2e : -INFINITY;
+  }
+}
+
 // Which (kv head, sequence) block x of the backward grid covers: dense x = batch * kv head
 // (the whole sequence), varlen x = sequence * head (a diagonal block of a B = 1 problem).
 struct BwdBlock {
@@ -381,7 +481,7 @@ cudaError_t set_smem(K kern, size_t bytes) {
 }
 
 cudaError_t launch_fwd_f32(const void* q, const void* k, const void* v, const FwdParams& p, bool causal,
-                           bool varlen, cudaStream_t stream) {
+                           int mode, cudaStream_t stream) {
   const size_t smem = sizeof(float) * (kTile * (p.d + 1) + kTile * p.d + kRows * p.d);
   const float* qf = static_cast<const float*>(q);
   const float* kf = static_cast<const float*>(k);
@@ -392,7 +492,11 @@ cudaError_t launch_fwd_f32(const void* q, const void* k, const void* v, const Fw
     kern<<<grid, 128, smem, stream>>>(qf, kf, vf, p);
     return cudaGetLastError();
   };
-  if (varlen) {
+  if (mode == kModeKv) {
+    const dim3 grid(p.B * p.Hq, (p.Nq + kRows - 1) / kRows, p.n_splits);
+    return causal ? run(fwd_f32_kv_kernel<true>, grid) : run(fwd_f32_kv_kernel<false>, grid);
+  }
+  if (mode == kModeVarlen) {
     const dim3 grid(p.Hq, (p.max_seqlen + kRows - 1) / kRows, p.nseq);
     return causal ? run(fwd_f32_kernel<true, true>, grid) : run(fwd_f32_kernel<false, true>, grid);
   }

@@ -59,6 +59,10 @@ WORKLOADS = {
                                   backward=True),
     "long_bf16": Workload("long_bf16 B1 Hq32 Hkv8 N32768 d128 bf16 causal fwd+bwd", "bf16", B=1,
                           Hq=32, Hkv=8, N=32768, d=128, causal=True, scale=None, backward=True),
+    # decode against a KV cache: one new token per sequence, caches of U[16384, 32768] keys
+    "decode_bf16": Workload("decode_bf16 B8 Hq32 Hkv8 Nq1 cache U[16384,32768] of 32768 d128 bf16", "bf16", B=8,
+                            Hq=32, Hkv=8, N=32768, d=128, causal=True, scale=None,
+                            extra={"Nq": 1, "lens": (16384, 32768)}),
 }
 
 
@@ -104,6 +108,38 @@ def varlen_inputs(lengths, H: int, d: int, dtype: str, seed: int = 0, with_dout:
     qkv = torch.randn(T, 3, H, d, generator=g, dtype=torch.float32).to(tdt)
     dout = torch.randn(T, H, d, generator=g, dtype=torch.float32).to(tdt) if with_dout else None
     return qkv, cu_seqlens_from_lengths(lengths), lengths, dout
+
+
+def kvcache_inputs(B, Hq, Hkv, Nq, Nk, d, dtype: str, lens=None, seed: int = 0):
+    """Q [B,Hq,Nq,d], K and V caches [B,Hkv,Nk,d] on the CPU in ``dtype``, and the cache
+    lengths as int32 [B] (None when ``lens`` is None).  ``lens`` is a list of lengths or an
+    inclusive range (lo, hi) drawn first from the generator, then Q, K, V."""
+    g = generator(seed)
+    if isinstance(lens, tuple):
+        lens = torch.randint(lens[0], lens[1] + 1, (B,), generator=g).tolist()
+    tdt = DTYPES[dtype]
+    q = torch.randn(B, Hq, Nq, d, generator=g, dtype=torch.float32).to(tdt)
+    k = torch.randn(B, Hkv, Nk, d, generator=g, dtype=torch.float32).to(tdt)
+    v = torch.randn(B, Hkv, Nk, d, generator=g, dtype=torch.float32).to(tdt)
+    return q, k, v, None if lens is None else torch.tensor([int(x) for x in lens], dtype=torch.int32)
+
+
+def kvcache_visible_pairs(lens, Nq: int, causal: bool) -> int:
+    """(query, key) pairs that enter the KV-cache forward: Nq * L per batch, or under the
+    bottom-right causal mask sum_i clamp(L - Nq + i + 1, 0, L)."""
+    total = 0
+    for L in lens:
+        L = int(L)
+        if causal:
+            total += sum(min(L, max(0, L - Nq + i + 1)) for i in range(Nq))
+        else:
+            total += Nq * L
+    return total
+
+
+def kvcache_fwd_flops(lens, Hq, Nq, d, causal: bool) -> float:
+    """Two contractions (Q.K^T and P.V) of 2 d FLOPs per visible pair per query head."""
+    return 4.0 * Hq * d * kvcache_visible_pairs(lens, Nq, causal)
 
 
 def fwd_flops(B, Hq, N, d, causal: bool) -> float:

@@ -54,8 +54,8 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED = 2,  /* valid but not provided: d not a multiple of 16 or above 128 */
   ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (launch, tensor map, ...) */
   ATTN_ERR_TIMEOUT = 4,      /* device: a pipeline wait exceeded its time limit; CTA stopped */
-  ATTN_ERR_DEVICE_INPUT = 5  /* device: cu_seqlens not non-decreasing from 0, or a sequence
-                                longer than max_seqlen */
+  ATTN_ERR_DEVICE_INPUT = 5  /* device: cu_seqlens not non-decreasing from 0, a sequence
+                                longer than max_seqlen, or a cache length outside [0, Nk] */
 } attn_status_t;
 
 #define ATTN_FLAG_OUT_F32 1u
@@ -152,6 +152,36 @@ attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout
                               const int32_t* cu_seqlens, int nseq, int total_tokens, int max_seqlen, void* dqkv,
                               void* workspace, size_t workspace_bytes, int H, int d, int causal, float scale,
                               attn_dtype_t dtype, unsigned flags, void* stream);
+
+/*
+ * KV cache / cross-attention forward: Nq queries per (batch, query head) against a cache of up to
+ * Nk keys per (batch, kv head) (the FlashAttention-T review, FAQ 4: at inference the KV cache is
+ * computed in blocks; its practical advice 2: the prefill and decode phases).  Decode is Nq = 1
+ * (or a few), prefill against a cache and cross-attention are larger Nq.
+ *   q              [B, Hq, Nq, d] (dtype)
+ *   k_cache, v_cache [B, Hkv, Nk, d] (dtype)
+ *   cache_seqlens  DEVICE int32 [B] or NULL: batch b's cache holds its first cache_seqlens[b]
+ *                  keys (0 <= cache_seqlens[b] <= Nk); NULL means Nk keys for every batch
+ *   o              [B, Hq, Nq, d] (dtype, or float32 with ATTN_FLAG_OUT_F32)
+ *   lse            [B, Hq, Nq] float32 (natural log), or NULL
+ *   causal         query i sees key j only when j <= L - Nq + i (L = the batch's cache length):
+ *                  the queries are the last Nq positions of the sequence (bottom-right
+ *                  alignment); with Nq == L this is the self-attention mask of attn_fwd
+ *   num_splits     key ranges per (batch, kv head), merged by their LSE (split-KV); 0 picks a
+ *                  count from the sizes (attn_fwd_kvcache_splits); at most one per 128 keys
+ *   workspace      DEVICE, at least attn_fwd_kvcache_workspace_bytes(...) bytes with the same
+ *                  sizes and num_splits, 256-byte aligned; contents on entry are ignored
+ * A query row that sees no key (an empty cache, or L < Nq under the causal mask) gets O = 0 and
+ * LSE = -inf.  B == 0 or Nq == 0 is a no-op.  A cache_seqlens entry outside [0, Nk] is detected
+ * on the device: that batch is treated as empty and attn_get_device_status() returns
+ * ATTN_ERR_DEVICE_INPUT.  Other argument rules are those of attn_fwd.
+ */
+int attn_fwd_kvcache_splits(int B, int Hq, int Hkv, int Nq, int Nk, int num_splits);
+size_t attn_fwd_kvcache_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits);
+attn_status_t attn_fwd_kvcache(const void* q, const void* k_cache, const void* v_cache, const int32_t* cache_seqlens,
+                               void* o, float* lse, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                               int Nq, int Nk, int d, int causal, float scale, int num_splits, attn_dtype_t dtype,
+                               unsigned flags, void* stream);
 
 /*
  * attn_bwd_noalloc -- the backward (same arguments, layouts and results as attn_bwd) for callers

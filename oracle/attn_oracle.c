@@ -403,8 +403,8 @@ int oracle_fwd_varlen(const double *qkv, const int32_t *cu, int nseq, int T, dou
 }
 
 /* KV-cache (and cross-attention) forward: Nq queries against a cache of up to Nk keys per
- * (batch, kv head) (FlashAttention-T review, 应用场景: blocked KV-cache computation for
- * inference; the prefill / decode split of the same review).  q [B,Hq,Nq,d], k and v
+ * (batch, kv head) (FlashAttention-T review, FAQ 4: at inference the KV cache is computed in
+ * blocks; its practical advice 2: the prefill and decode phases).  q [B,Hq,Nq,d], k and v
  * [B,Hkv,Nk,d], lens [B] (NULL: every cache holds Nk keys; else 0 <= lens[b] <= Nk),
  * o [B,Hq,Nq,d], lse [B,Hq,Nq] (may be NULL).
  *

@@ -156,3 +156,42 @@ def test_bwd_varlen_workspace_and_validation(lib):
     assert f(H=0) == _lib.ATTN_ERR_INVALID_ARG
     assert f(d=40) == _lib.ATTN_ERR_UNSUPPORTED
     assert f(flags=2) == _lib.ATTN_ERR_INVALID_ARG
+
+
+def test_kvcache_splits_workspace_and_validation(lib):
+    S = _lib.attn_fwd_kvcache_splits
+    # 0 = about eight work items per SM of a 152-SM GPU: 64 (batch, kv head) blocks of one row
+    # block over 256 key tiles -> 19 ranges of 14 tiles
+    assert S(8, 32, 8, 1, 32768, 0) == 19
+    assert S(1, 8, 8, 1, 300, 0) == 3           # at most one range per 128-key tile
+    assert S(2, 4, 2, 1, 1000, 5) == 4          # 8 tiles in ranges of 2: the empty 5th is dropped
+    assert S(1, 1, 1, 1, 128, 7) == 1
+    assert S(1, 1, 1, 1, 0, 0) == 1             # an empty cache still has one (empty) range
+    assert S(1, 3, 2, 1, 64, 0) == 0 and S(1, 2, 1, 0, 64, 0) == 0 and S(1, 2, 1, 1, 64, -1) == 0
+    r256 = lambda x: (x + 255) // 256 * 256
+    ws = _lib.attn_fwd_kvcache_workspace_bytes(2, 4, 2, 3, 1000, 64, 5)
+    rows = 2 * 4 * 3
+    assert ws == r256(4 * rows * 64 * 4) + r256(4 * rows * 4)
+
+    def f(**kw):
+        a = dict(q=4096, k=4096, v=4096, lens=None, o=4096, lse=None, ws=4096, wsb=ws, B=2, Hq=4, Hkv=2, Nq=3,
+                 Nk=1000, d=64, causal=1, scale=0.0, splits=5, dtype=_lib.ATTN_BF16, flags=0)
+        a.update(kw)
+        return _lib.attn_fwd_kvcache(a["q"], a["k"], a["v"], a["lens"], a["o"], a["lse"], a["ws"], a["wsb"], a["B"],
+                                     a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["d"], a["causal"], a["scale"],
+                                     a["splits"], a["dtype"], a["flags"], None)
+    assert f(B=0) == _lib.ATTN_OK and f(Nq=0) == _lib.ATTN_OK
+    assert f(q=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(k=None) == _lib.ATTN_ERR_INVALID_ARG and f(v=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(k=4100) == _lib.ATTN_ERR_INVALID_ARG      # not 16-byte aligned
+    assert f(lens=4098) == _lib.ATTN_ERR_INVALID_ARG   # not 4-byte aligned
+    assert f(lse=4098) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(ws=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(ws=4096 + 128) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(wsb=ws - 1) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(Hq=3) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(Nk=-1) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(splits=-1) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(d=40) == _lib.ATTN_ERR_UNSUPPORTED
+    assert f(flags=2) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(scale=-1.0) == _lib.ATTN_ERR_INVALID_ARG
