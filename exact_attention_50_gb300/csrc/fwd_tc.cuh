@@ -109,13 +109,16 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int idx) {
   it.j0 = 0;
   it.split = 0;
   if constexpr (MODE == kModeKv) {
-    // later row blocks first (under the causal mask they see the most keys), then (batch,
-    // kv head), then the key range
-    const int per_rb = p.B * p.Hkv * p.n_splits;
+    // later row blocks first (under the causal mask they see the most keys), then the key
+    // range (first ranges first: they are full, the last ones short or empty), then (batch,
+    // kv head).  A CTA takes every gridDim.x-th item, so it gets a mix of ranges and of
+    // caches of different lengths, and the light items come last.
+    const int bhs = p.B * p.Hkv;
+    const int per_rb = bhs * p.n_splits;
     it.qt = p.n_qtiles - 1 - idx / per_rb;
     const int rem = idx % per_rb;
-    const int bh = rem / p.n_splits;
-    it.split = rem % p.n_splits;
+    it.split = rem / bhs;
+    const int bh = rem % bhs;
     it.b = bh / p.Hkv;
     it.h = bh % p.Hkv;
     it.seq_start = 0;
