@@ -44,6 +44,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded CPU-baseline sample time")
+    ap.add_argument("--deterministic", action="store_true", help="backward with bitwise reproducible dQ")
     return ap.parse_args(argv)
 
 
@@ -283,6 +284,7 @@ def run_ours(args, rank, world, local):
     sp = stream.cuda_stream
     dt_code = {"f32": _lib.ATTN_F32, "f16": _lib.ATTN_F16, "bf16": _lib.ATTN_BF16}[wl.dtype]
     scale = 0.0 if wl.scale is None else float(wl.scale)
+    bwd_flags = _lib.ATTN_FLAG_DETERMINISTIC if args.deterministic else 0
 
     lengths = None
     kv_bytes = None
@@ -342,7 +344,7 @@ def run_ours(args, rank, world, local):
             bwd_calls = [
                 lambda: lib.attn_bwd_varlen(qkv.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                                             cu.data_ptr(), len(lengths), T, maxlen, dqkv.data_ptr(), ws.data_ptr(),
-                                            nbytes, wl.Hq, wl.d, int(wl.causal), scale, dt_code, 0, sp),
+                                            nbytes, wl.Hq, wl.d, int(wl.causal), scale, dt_code, bwd_flags, sp),
             ]
     else:
         q_h, k_h, v_h, do_h = W.dense_inputs(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.dtype, seed=0,
@@ -372,7 +374,7 @@ def run_ours(args, rank, world, local):
                                              wl.N, wl.d, dt_code, sp),
                 lambda: lib.attn_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), nbytes,
-                                          *args_dims, int(wl.causal), scale, dt_code, 0, sp),
+                                          *args_dims, int(wl.causal), scale, dt_code, bwd_flags, sp),
                 lambda: lib.attn_bwd_finish(dq.data_ptr(), ws.data_ptr(), nbytes, wl.B, wl.Hq, wl.N, wl.d, scale,
                                             dt_code, 0, sp),
             ]
@@ -514,6 +516,8 @@ def run_ours(args, rank, world, local):
                "head_dim": wl.d, "causal": wl.causal, "parallelism": f"replicas x{world}",
                "l2": "inputs larger than L2 (no flush)" if not wl.varlen else "inputs larger than L2 (no flush)",
                "step": "fwd + bwd (prepare, main, finish)" if bwd_calls else "fwd"}
+        if args.deterministic:
+            cfg["deterministic"] = True
         if wl.varlen:
             cfg["total_tokens"] = sum(lengths)
         if kv_bytes is not None:

@@ -16,6 +16,7 @@ ATTN_ERR_CUDA = 3
 ATTN_ERR_TIMEOUT = 4
 ATTN_ERR_DEVICE_INPUT = 5
 ATTN_FLAG_OUT_F32 = 1
+ATTN_FLAG_DETERMINISTIC = 2
 
 _lib = None
 

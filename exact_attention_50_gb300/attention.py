@@ -75,8 +75,13 @@ def fwd(q, k, v, causal: bool, scale=None, out_f32: bool = False, with_lse: bool
     return o, lse
 
 
-def bwd(q, k, v, o, lse, dout, causal: bool, scale=None, out_f32: bool = False, workspace=None):
-    """Dense backward.  Returns (dq, dk, dv)."""
+def _bwd_flags(out_f32: bool, deterministic: bool) -> int:
+    return (_lib.ATTN_FLAG_OUT_F32 if out_f32 else 0) | (_lib.ATTN_FLAG_DETERMINISTIC if deterministic else 0)
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool, scale=None, out_f32: bool = False, workspace=None,
+        deterministic: bool = False):
+    """Dense backward.  Returns (dq, dk, dv).  deterministic: dq bitwise reproducible (slower)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _require(t, n, q.dtype)
     _require(lse, "lse", torch.float32)
@@ -94,7 +99,7 @@ def bwd(q, k, v, o, lse, dout, causal: bool, scale=None, out_f32: bool = False, 
     st = _lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
                        B, Hq, Hkv, N, d, causal, _scale_arg(scale), _dtype_code(q),
-                       _lib.ATTN_FLAG_OUT_F32 if out_f32 else 0, _stream())
+                       _bwd_flags(out_f32, deterministic), _stream())
     _lib._check(st, "attn_bwd")
     return dq, dk, dv
 
@@ -121,7 +126,7 @@ def fwd_varlen(qkv, cu_seqlens, max_seqlen: int, causal: bool, scale=None, out_f
 
 
 def bwd_varlen(qkv, out, lse, dout, cu_seqlens, max_seqlen: int, causal: bool, scale=None, out_f32: bool = False,
-               workspace=None):
+               workspace=None, deterministic: bool = False):
     """Packed varlen backward.  qkv [T,3,H,d], out / dout [T,H,d], lse [H,T] (from fwd_varlen),
     cu_seqlens int32 [nseq+1] (device).  Returns dqkv [T,3,H,d]."""
     _require(qkv, "qkv")
@@ -140,7 +145,7 @@ def bwd_varlen(qkv, out, lse, dout, cu_seqlens, max_seqlen: int, causal: bool, s
     st = _lib.attn_bwd_varlen(qkv.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(), cu_seqlens.data_ptr(),
                               nseq, T, int(max_seqlen), dqkv.data_ptr(), workspace.data_ptr(), workspace.numel(), H,
                               d, causal, _scale_arg(scale), _dtype_code(qkv),
-                              _lib.ATTN_FLAG_OUT_F32 if out_f32 else 0, _stream())
+                              _bwd_flags(out_f32, deterministic), _stream())
     _lib._check(st, "attn_bwd_varlen")
     return dqkv
 
@@ -187,37 +192,39 @@ def fwd_kvcache(q, k_cache, v_cache, cache_seqlens=None, causal: bool = False, s
 
 class _AttnFn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, causal, scale):
+    def forward(ctx, q, k, v, causal, scale, deterministic):
         o, lse = fwd(q, k, v, causal, scale)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.causal, ctx.scale = causal, scale
+        ctx.causal, ctx.scale, ctx.deterministic = causal, scale, deterministic
         return o
 
     @staticmethod
     def backward(ctx, dout):
         q, k, v, o, lse = ctx.saved_tensors
-        dq, dk, dv = bwd(q, k, v, o, lse, dout.contiguous(), ctx.causal, ctx.scale)
-        return dq, dk, dv, None, None
+        dq, dk, dv = bwd(q, k, v, o, lse, dout.contiguous(), ctx.causal, ctx.scale, deterministic=ctx.deterministic)
+        return dq, dk, dv, None, None, None
 
 
-def flash_attention(q, k, v, causal: bool = True, scale=None):
-    """Exact attention of [B,Hq,N,d] queries over [B,Hkv,N,d] keys/values (Hq % Hkv == 0)."""
-    return _AttnFn.apply(q, k, v, causal, scale)
+def flash_attention(q, k, v, causal: bool = True, scale=None, deterministic: bool = False):
+    """Exact attention of [B,Hq,N,d] queries over [B,Hkv,N,d] keys/values (Hq % Hkv == 0).
+    deterministic makes the backward's dq bitwise reproducible (slower)."""
+    return _AttnFn.apply(q, k, v, causal, scale, bool(deterministic))
 
 
 class _VarlenFn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, qkv, cu_seqlens, max_seqlen, causal, scale):
+    def forward(ctx, qkv, cu_seqlens, max_seqlen, causal, scale, deterministic):
         out, lse = fwd_varlen(qkv, cu_seqlens, max_seqlen, causal, scale)
         ctx.save_for_backward(qkv, out, lse, cu_seqlens)
-        ctx.max_seqlen, ctx.causal, ctx.scale = max_seqlen, causal, scale
+        ctx.max_seqlen, ctx.causal, ctx.scale, ctx.deterministic = max_seqlen, causal, scale, deterministic
         return out
 
     @staticmethod
     def backward(ctx, dout):
         qkv, out, lse, cu_seqlens = ctx.saved_tensors
-        dqkv = bwd_varlen(qkv, out, lse, dout.contiguous(), cu_seqlens, ctx.max_seqlen, ctx.causal, ctx.scale)
-        return dqkv, None, None, None, None
+        dqkv = bwd_varlen(qkv, out, lse, dout.contiguous(), cu_seqlens, ctx.max_seqlen, ctx.causal, ctx.scale,
+                          deterministic=ctx.deterministic)
+        return dqkv, None, None, None, None, None
 
 
 def flash_attn_varlen_qkvpacked_func(qkv, cu_seqlens, max_seqlen, dropout_p=0.0, softmax_scale=None,
@@ -242,4 +249,5 @@ def flash_attn_varlen_qkvpacked_func(qkv, cu_seqlens, max_seqlen, dropout_p=0.0,
         raise ValueError("Bad batch size")
     if qkv.shape[0] != int(cu_seqlens[-1].item()):
         raise ValueError("Token count mismatch")
-    return _VarlenFn.apply(qkv, cu_seqlens.to(torch.int32), int(max_seqlen), bool(causal), softmax_scale)
+    return _VarlenFn.apply(qkv, cu_seqlens.to(torch.int32), int(max_seqlen), bool(causal), softmax_scale,
+                           bool(deterministic))

@@ -204,7 +204,7 @@ attn_status_t attn_fwd_varlen(const void* qkv, const int32_t* cu_seqlens, int ns
 size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int d) {
   if (B <= 0 || Hq <= 0 || N <= 0 || d <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * N;
-  return round256(rows * d * sizeof(float)) + round256(rows * sizeof(float));
+  return round256(rows * d * sizeof(float)) + 2 * round256(rows * sizeof(float));
 }
 
 namespace {
@@ -215,7 +215,7 @@ attn_status_t bwd_setup(BwdParams* p, void* workspace, size_t workspace_bytes, i
   attn_status_t st = check_common(d, scale, dtype);
   if (st != ATTN_OK) return st;
   if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (flags & ~ATTN_FLAG_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~(ATTN_FLAG_OUT_F32 | ATTN_FLAG_DETERMINISTIC)) return ATTN_ERR_INVALID_ARG;
   if (B == 0 || N == 0) return ATTN_OK;
   if (!workspace || !aligned(workspace, 256)) return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, N, d)) return ATTN_ERR_INVALID_ARG;
@@ -224,6 +224,8 @@ attn_status_t bwd_setup(BwdParams* p, void* workspace, size_t workspace_bytes, i
   const size_t rows = static_cast<size_t>(B) * Hq * N;
   p->dq_acc = static_cast<float*>(workspace);
   p->delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * d * sizeof(float)));
+  p->dq_turn = reinterpret_cast<int*>(reinterpret_cast<char*>(p->delta) + round256(rows * sizeof(float)));
+  p->deterministic = (flags & ATTN_FLAG_DETERMINISTIC) ? 1 : 0;
   p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->N = N; p->d = d; p->G = Hq / Hkv;
   p->n_ktiles = (N + attn::kBN - 1) / attn::kBN;
   const BwdParams::Rows dense{d, static_cast<long long>(N) * d};
@@ -315,7 +317,7 @@ attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout
   attn_status_t st = check_common(d, scale, dtype);
   if (st != ATTN_OK) return st;
   if (nseq < 0 || total_tokens < 0 || max_seqlen < 0 || H <= 0) return ATTN_ERR_INVALID_ARG;
-  if (flags & ~ATTN_FLAG_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~(ATTN_FLAG_OUT_F32 | ATTN_FLAG_DETERMINISTIC)) return ATTN_ERR_INVALID_ARG;
   if (nseq == 0) return total_tokens == 0 ? ATTN_OK : ATTN_ERR_INVALID_ARG;
   if (!cu_seqlens || !aligned(cu_seqlens, 4)) return ATTN_ERR_INVALID_ARG;
   if (total_tokens == 0) return ATTN_OK;  // every sequence is empty

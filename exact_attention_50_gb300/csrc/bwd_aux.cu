@@ -2,7 +2,7 @@
 //
 // preprocess:  D_i = sum_c dO[i,c] * O[i,c] in fp32 (equal to sum_j P_ij dP_ij, the row term
 //              of dS_ij = P_ij (dP_ij - D_i)), and, for the tensor-core path, zero the fp32 dQ
-//              accumulator that the main kernel reduces into.
+//              accumulator that the main kernel reduces into and its per-tile turn counters.
 // postprocess: dQ = scale * dQacc, rounded to the output dtype (or kept fp32 on request).
 // Both are HBM-bound streams with 16-byte accesses.
 #include <cuda_bf16.h>
@@ -29,7 +29,8 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return _
 template <typename T, bool CONTIG, int GS>
 __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dout,
                                                          float* __restrict__ delta, float* __restrict__ dq_acc,
-                                                         long rows, int N, BwdParams::Rows lay, int d) {
+                                                         int* __restrict__ turn, long rows, int N, BwdParams::Rows lay,
+                                                         int d) {
   constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte load
   constexpr int kRowsPerStep = 32 / GS;
   constexpr int kUnroll = 4;
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ o
       if (r < rows) {
         if (g == 0) delta[r] = acc;
         if (dq_acc) {
+          if (g == 0) turn[r] = 0;
           float4* z = reinterpret_cast<float4*>(dq_acc + r * d);
           for (int c = g; c < d / 4; c += GS) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -165,13 +167,13 @@ void preprocess_g(const BwdParams& p, float* acc, long rows, int grid, cudaStrea
   const T* g = static_cast<const T*>(p.dout);
   const int lanes = p.d / (16 / static_cast<int>(sizeof(T)));  // 16-byte vectors per row: 2 .. 32
   if (lanes <= 4)
-    preprocess_kernel<T, CONTIG, 4><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, rows, p.N, p.lay_o, p.d);
+    preprocess_kernel<T, CONTIG, 4><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, p.dq_turn, rows, p.N, p.lay_o, p.d);
   else if (lanes <= 8)
-    preprocess_kernel<T, CONTIG, 8><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, rows, p.N, p.lay_o, p.d);
+    preprocess_kernel<T, CONTIG, 8><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, p.dq_turn, rows, p.N, p.lay_o, p.d);
   else if (sizeof(T) == 2 || lanes <= 16)  // 16-bit rows of d <= 128 take at most 16 vectors
-    preprocess_kernel<T, CONTIG, 16><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, rows, p.N, p.lay_o, p.d);
+    preprocess_kernel<T, CONTIG, 16><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, p.dq_turn, rows, p.N, p.lay_o, p.d);
   else if constexpr (sizeof(T) == 4)
-    preprocess_kernel<T, CONTIG, 32><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, rows, p.N, p.lay_o, p.d);
+    preprocess_kernel<T, CONTIG, 32><<<grid, 256, 0, stream>>>(o, g, p.delta, acc, p.dq_turn, rows, p.N, p.lay_o, p.d);
 }
 
 template <typename T>

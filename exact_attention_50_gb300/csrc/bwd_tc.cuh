@@ -381,6 +381,14 @@ __global__ void __launch_bounds__(512, 1)
       mbar_arrive_warp(stage_full);
       if (warp == 8 && lane == 0) {
         if (!mbar_wait(stage_full, it & 1, abort_flag, p.status)) { ok = false; }
+        // deterministic: key tile kt adds into this dQ tile after key tiles 0 .. kt-1 (the
+        // tiles of the same sequence that also reach it, launched before this CTA)
+        if (ok && p.deterministic) {
+          if (wait_turn(p.dq_turn + row0, kt, abort_flag, p.status))
+            fence_async_global();  // the reductions below come after the turn was seen
+          else
+            ok = false;
+        }
         if (ok) {
           if (L::kLoStageChunks > 0) {
             for (int c = L::kOwnStageChunks; c < DP / 32; ++c)
@@ -396,6 +404,11 @@ __global__ void __launch_bounds__(512, 1)
           }
           bulk_wait_read<0>();
           mbar_arrive(stage_free);
+          if (p.deterministic) {
+            bulk_wait_all();       // the reductions have been performed ...
+            fence_async_global();  // ... before the turn passes to key tile kt + 1
+            red_release_gpu_add(p.dq_turn + row0, 1);
+          }
         }
       }
       __syncwarp();

@@ -78,6 +78,9 @@ struct BwdParams {
   void* dv;
   float* dq_acc;   // workspace [B,Hq,N,d] fp32
   float* delta;    // workspace [B,Hq,N] fp32: D_i = dO_i . O_i
+  int* dq_turn;    // workspace [B,Hq,N] int32, zeroed with dq_acc: at the first row of each
+                   // 128-row dQ tile, the key tiles that have added into that tile
+  int deterministic;  // add dQ tiles in key-tile order (ATTN_FLAG_DETERMINISTIC)
   unsigned* status;
   int B, Hq, Hkv, N, d, G;
   int n_ktiles;

@@ -9,7 +9,8 @@
 // review, FAQ 4; the merge is the same online-softmax rescaling as across key tiles, its best
 // practice 4.)
 //
-// One warp per output row; lane l owns columns 4l .. 4l+3 (d <= 128).  Which ranges hold data
+// One warp per output row; lane l owns columns 4l .. 4l+3 (d <= 128), and the loads of eight
+// ranges are issued before any is used (the ranges' parts sit far apart).  Which ranges hold data
 // follows from the forward's work split (kv_needed_keys): a range past the block's last
 // visible key was never computed and is not read.
 #include <cuda_bf16.h>
@@ -63,19 +64,32 @@ __global__ void __launch_bounds__(256) kv_combine_kernel(const FwdParams p) {
     }
     const int need_tiles = (kv_needed_keys(L, p.Nq, p.R, rr / 128, CAUSAL) + 127) / 128;
     const int nv = min(p.n_splits, (need_tiles + p.tiles_per_split - 1) / p.tiles_per_split);
+    // the largest range LSE: lanes over the ranges, then a warp reduction
     float mx = -INFINITY;
-    for (int s = 0; s < nv; ++s) mx = fmaxf(mx, p.lse_part[s * rows + r]);
+    for (int s = lane; s < nv; s += 32) mx = fmaxf(mx, p.lse_part[s * rows + r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // weighted sum of the range outputs, eight ranges' loads in flight at a time
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, wsum = 0.f;
     if (mx != -INFINITY) {
-      for (int s = 0; s < nv; ++s) {
-        const float w = expf(p.lse_part[s * rows + r] - mx);
-        wsum += w;
-        if (col_ok && w > 0.f) {
-          const float4 o = *reinterpret_cast<const float4*>(p.o_part + (s * rows + r) * p.d + lane * 4);
-          a0 = fmaf(w, o.x, a0);
-          a1 = fmaf(w, o.y, a1);
-          a2 = fmaf(w, o.z, a2);
-          a3 = fmaf(w, o.w, a3);
+      for (int s0 = 0; s0 < nv; s0 += 8) {
+        float ls[8];
+        float4 os[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int s = s0 + u;
+          ls[u] = s < nv ? p.lse_part[s * rows + r] : -INFINITY;
+          os[u] = (s < nv && col_ok) ? *reinterpret_cast<const float4*>(p.o_part + (s * rows + r) * p.d + lane * 4)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float w = expf(ls[u] - mx);  // 0 for ranges past nv and for rows empty in a range
+          wsum += w;
+          a0 = fmaf(w, os[u].x, a0);
+          a1 = fmaf(w, os[u].y, a1);
+          a2 = fmaf(w, os[u].z, a2);
+          a3 = fmaf(w, os[u].w, a3);
         }
       }
     }

@@ -164,6 +164,35 @@ __device__ __forceinline__ void bulk_wait_read() {
 // Waits until every committed bulk group has completed (its writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Orders this thread's generic-proxy and async-proxy (bulk copy) accesses to global memory.
+__device__ __forceinline__ void fence_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded wait (one thread) until the counter at p reaches `target` (counters only grow).
+// Returns false after raising the abort flag, and on a timeout the device status.
+__device__ __forceinline__ bool wait_turn(const int* p, int target, uint32_t abort_flag, unsigned* status) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    __nanosleep(100);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if (abort_read(abort_flag)) return false;
+    if (globaltimer() - t0 > kWaitTimeoutNs) {
+      raise_status(status, ATTN_ERR_TIMEOUT);
+      abort_set(abort_flag, 1);
+      return false;
+    }
+  }
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (tensor core, TMA).
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -59,6 +59,12 @@ typedef enum {
 } attn_status_t;
 
 #define ATTN_FLAG_OUT_F32 1u
+/* Backward only (attn_bwd, attn_bwd_main, attn_bwd_varlen, attn_bwd_noalloc): dq is bitwise
+ * reproducible from run to run.  The key tiles add their parts of each 128-row dQ tile into the
+ * fp32 accumulator in key-tile order (each waits, on the device and bounded, for the one
+ * before it) instead of in the order they arrive; slower.  dk, dv and the fp32 path are
+ * reproducible in either mode. */
+#define ATTN_FLAG_DETERMINISTIC 2u
 
 /*
  * Forward.
@@ -91,7 +97,8 @@ attn_status_t attn_fwd_varlen(const void* qkv, const int32_t* cu_seqlens, int ns
                               attn_dtype_t dtype, unsigned flags, void* stream);
 
 /* Bytes of device workspace attn_bwd needs for these sizes (an fp32 dQ accumulator
- * [B,Hq,N,d] and the fp32 row terms D_i = dO_i . O_i [B,Hq,N], each 256-byte aligned). */
+ * [B,Hq,N,d], the fp32 row terms D_i = dO_i . O_i [B,Hq,N] and int32 turn counters [B,Hq,N]
+ * for ATTN_FLAG_DETERMINISTIC, each 256-byte aligned). */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int d);
 
 /*
@@ -128,8 +135,9 @@ attn_status_t attn_bwd_main(const void* q, const void* k, const void* v, const v
 attn_status_t attn_bwd_finish(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int N, int d,
                               float scale, attn_dtype_t dtype, unsigned flags, void* stream);
 
-/* Bytes of device workspace attn_bwd_varlen needs (an fp32 dQ accumulator [H, total_tokens, d]
- * and the fp32 row terms [H, total_tokens], each 256-byte aligned). */
+/* Bytes of device workspace attn_bwd_varlen needs (an fp32 dQ accumulator [H, total_tokens, d],
+ * the fp32 row terms [H, total_tokens] and int32 turn counters [H, total_tokens], each
+ * 256-byte aligned). */
 size_t attn_bwd_varlen_workspace_bytes(int total_tokens, int H, int d);
 
 /*

@@ -103,7 +103,7 @@ def test_bwd_workspace_and_validation(lib):
     ws = _lib.attn_bwd_workspace_bytes(2, 4, 100, 64)
     rows = 2 * 4 * 100
     r256 = lambda x: (x + 255) // 256 * 256
-    assert ws == r256(rows * 64 * 4) + r256(rows * 4)
+    assert ws == r256(rows * 64 * 4) + 2 * r256(rows * 4)  # dQ acc, D, turn counters
     assert _lib.attn_bwd_workspace_bytes(0, 4, 100, 64) == 0
     args = [4096] * 10 + [ws, 2, 4, 2, 100, 64, 1, 0.0, _lib.ATTN_BF16, 0, None]
     small = list(args)
@@ -155,7 +155,7 @@ def test_bwd_varlen_workspace_and_validation(lib):
     assert f(wsb=ws - 1) == _lib.ATTN_ERR_INVALID_ARG
     assert f(H=0) == _lib.ATTN_ERR_INVALID_ARG
     assert f(d=40) == _lib.ATTN_ERR_UNSUPPORTED
-    assert f(flags=2) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(flags=4) == _lib.ATTN_ERR_INVALID_ARG
 
 
 def test_kvcache_splits_workspace_and_validation(lib):
