@@ -155,6 +155,11 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   if (!make_dense_map(&maps.q, q, dtype, B * Hq, N, d) || !make_dense_map(&maps.k, k, dtype, B * Hkv, N, d) ||
       !make_dense_map(&maps.v, v, dtype, B * Hkv, N, d))
     return ATTN_ERR_CUDA;
+  // the epilogue's tile stores (16-bit output); an fp32 output is stored by the threads
+  if (p.out_f32)
+    maps.o = maps.q;
+  else if (!make_dense_map(&maps.o, o, dtype, B * Hq, N, d))
+    return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_fwd_tc(maps, p, dtype, causal != 0, attn::kModeDense, s));
 }
 
@@ -198,6 +203,7 @@ attn_status_t attn_fwd_varlen(const void* qkv, const int32_t* cu_seqlens, int ns
   if (!make_packed_map(&maps.q, qkv, dtype, total_tokens, H, d)) return ATTN_ERR_CUDA;
   maps.k = maps.q;
   maps.v = maps.q;
+  maps.o = maps.q;  // unused: varlen rows are stored by the threads
   return from_cuda(attn::launch_fwd_tc(maps, p, dtype, causal != 0, attn::kModeVarlen, s));
 }
 
@@ -459,6 +465,7 @@ attn_status_t attn_fwd_kvcache(const void* q, const void* k_cache, const void* v
           !make_dense_map(&maps.k, k_cache, dtype, static_cast<int>(bh), Nk, d) ||
           !make_dense_map(&maps.v, v_cache, dtype, static_cast<int>(bh), Nk, d))
         return ATTN_ERR_CUDA;
+      maps.o = maps.q;  // unused: the partials are stored by the threads
       e = attn::launch_fwd_tc(maps, p, dtype, causal != 0, attn::kModeKv, s);
     }
     if (e != cudaSuccess) return ATTN_ERR_CUDA;

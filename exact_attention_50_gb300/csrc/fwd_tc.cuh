@@ -64,12 +64,13 @@ constexpr unsigned kPolyPairs = 0x00u;
 
 template <int DP>
 struct FwdLayout {
-  // For d = 128 one Q tile and three K and three V tiles in flight (224 KB in all): an L2
-  // load takes up to ~3000 cycles when every SM streams K and V, about two tiles of work.
-  // d = 64 double-buffers Q as well (the next item's Q loads while the current one is used).
-  static constexpr int kStagesQ = DP == 128 ? 1 : 2;
+  // For d = 128 two Q tiles, three K and two V tiles in flight (224 KB in all): an L2 load
+  // takes up to ~3000 cycles when every SM streams K and V, about two tiles of work.  The
+  // second Q slot lets the next item's Q load while the current item's slot, once its last S
+  // has run, stages the item's output tile for the tile stores.  (1 Q + 3 V measured the same.)
+  static constexpr int kStagesQ = 2;
   static constexpr int kStagesK = DP == 128 ? 3 : 4;
-  static constexpr int kStagesV = DP == 128 ? 3 : 4;
+  static constexpr int kStagesV = DP == 128 ? 2 : 4;
   static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 64 elements x 2 B
   static constexpr int kTileBytes = (DP / 64) * kChunkBytes;
   static constexpr int kOffQ = 0;
@@ -78,14 +79,14 @@ struct FwdLayout {
   static constexpr int kOffX = kOffV + kStagesV * kTileBytes;  // exchange [2 slots][2 groups][128 rows]
   static constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
   // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
-  // s_free[2], p_full[2], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain
-  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1;
+  // s_free[2], p_full[2], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain, o_staged
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base (u32), abort flag (int)
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColP = 256, kColO = 384;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -205,11 +206,17 @@ struct TileCursor {
 };
 
 template <typename T, int DP, bool CAUSAL, int MODE>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p, int n_items) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdParams p, int n_items) {
   constexpr bool VARLEN = MODE == kModeVarlen;
   constexpr bool KV = MODE == kModeKv;
+  // Dense 16-bit output: the softmax warps stage each item's O tile in the item's Q slot (free
+  // once its last S has run) and warp 10 writes it with tile stores, then frees the slot.
+  // Otherwise (varlen rows must not spill into the next sequence; fp32 or KV-cache partials)
+  // the softmax warps store their rows themselves and the last S frees the Q slot.
+  const bool tile_epi = MODE == kModeDense && !p.out_f32;
   using L = FwdLayout<DP>;
   constexpr int SQ = L::kStagesQ, SK = L::kStagesK, SV = L::kStagesV;
   constexpr int kChunks = DP / 64;
@@ -241,6 +248,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* o_free = pv_done + 2;
   uint64_t* xch = o_free + 1;       // [quadrant][slot]: row-max / row-sum exchange, warps q and q + 4
   uint64_t* drain = xch + 8;
+  uint64_t* o_staged = drain + 1;  // the softmax warps have written the item's O tile (tile_epi)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
@@ -268,6 +276,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(o_free, 8);
     for (int i = 0; i < 8; ++i) mbar_init(xch + i, 2);  // the two warps of a row quadrant
     mbar_init(drain, 1);
+    mbar_init(o_staged, 8);
     abort_set(abort_flag, 0);
     mbar_init_fence();
   }
@@ -442,7 +451,7 @@ __global__ void __launch_bounds__(320, 1)
             issue_s(ts, qs);
             mma_commit(k_empty + ts % SK);
             ++ns;
-            if (ns == n) mma_commit(q_empty + qs);
+            if (ns == n && !tile_epi) mma_commit(q_empty + qs);
             progress = true;
           }
           const uint32_t tp = t0 + np;
@@ -474,6 +483,26 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(drain);  // every MMA issued so far completes before this arrives
         mbar_drain(drain, 0);
       }
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ================================================================ output tile stores
+    if (lane == 0 && tile_epi) {
+      tma_prefetch_desc(&tmO);
+      uint32_t ic = 0;
+      for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
+        const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
+        if (!it.valid) continue;
+        const uint32_t qs = ic % SQ;
+        if (!mbar_wait(o_staged, ic & 1, abort_flag, p.status)) break;
+        for (int c = 0; c < kChunks; ++c)
+          tma_store_3d(&tmO, sQ + qs * L::kTileBytes + c * L::kChunkBytes, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(q_empty + qs);  // the slot may take the Q of the item after next
+        ++ic;
+      }
+      bulk_wait_all();  // the stores are complete before the CTA ends
     }
     __syncwarp();
   } else {
@@ -648,8 +677,39 @@ __global__ void __launch_bounds__(320, 1)
       const bool o_f32 = KV || p.out_f32;
       void* const o_base = KV ? static_cast<void*>(p.o_part) : p.o;
       uint32_t r[32];
+      if (tile_epi) {
+        // this group's DP / 2 columns of row `row` (from column grp * DP / 2) into the item's Q
+        // slot, in the 128-byte swizzled layout of the output map's {64, 128} boxes: column
+        // col lands in box col / 64, 16-byte granule (col % 64) / 8; rows and columns past the
+        // tensor are clipped by the store
+        constexpr int kHalf = DP / 2;
+        uint8_t* srow = sQ + (ic % SQ) * L::kTileBytes + ((grp * kHalf) / 64) * L::kChunkBytes + row * 128;
+        const int gran0 = ((grp * kHalf) % 64) / 8;
 #pragma unroll
-      for (int c = 0; c < DP / 64; ++c) {
+        for (int c = 0; c < DP / 64; ++c) {
+          tmem_ld32(tO + c * 32, r);
+          tmem_ld_wait();
+          tmem_reg_fence(r);
+          if (c == DP / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive_warp(o_free);  // O is in registers: the next item may overwrite it
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 v;
+            v.x = Elem<T>::pack(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+            v.y = Elem<T>::pack(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+            v.z = Elem<T>::pack(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+            v.w = Elem<T>::pack(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+            const int gran = gran0 + c * 4 + i;
+            *reinterpret_cast<uint4*>(srow + ((gran ^ (row & 7)) << 4)) = v;
+          }
+        }
+        fence_async_smem();
+        mbar_arrive_warp(o_staged);
+      }
+#pragma unroll
+      for (int c = 0; c < (tile_epi ? 0 : DP / 64); ++c) {
         tmem_ld32(tO + c * 32, r);
         tmem_ld_wait();
         tmem_reg_fence(r);
@@ -680,8 +740,10 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive_warp(o_free);
+      if (!tile_epi) {
+        tc_fence_before();
+        mbar_arrive_warp(o_free);
+      }
       if (grp == 0 && valid && (KV || p.lse)) {
         const float lse = (m + __log2f(l_all)) * 0.69314718055994531f;
         if constexpr (KV)
@@ -726,7 +788,7 @@ cudaError_t launch_fwd_tc_t(const FwdMaps& maps, const FwdParams& p, cudaStream_
   const long items = heads * p.n_qtiles;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
-  kern<<<grid, L::kThreads, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, p, static_cast<int>(items));
+  kern<<<grid, L::kThreads, L::kSmemAlloc, stream>>>(maps.q, maps.k, maps.v, maps.o, p, static_cast<int>(items));
   return cudaGetLastError();
 }
 

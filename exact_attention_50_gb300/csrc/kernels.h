@@ -51,6 +51,7 @@ __host__ __device__ inline int kv_needed_keys(int L, int Nq, int R, int rb, bool
 // Boxes are {64, 128(, 1)} with 128-byte swizzle; rows past a map's extent load as zeros.
 struct FwdMaps {
   CUtensorMap q, k, v;
+  CUtensorMap o;  // dense 16-bit output: the epilogue's tile stores ({d, N, B*Hq}, like q)
 };
 
 // Work-item layouts of the forward kernels.
