@@ -203,7 +203,11 @@ attn_status_t attn_fwd_varlen(const void* qkv, const int32_t* cu_seqlens, int ns
   if (!make_packed_map(&maps.q, qkv, dtype, total_tokens, H, d)) return ATTN_ERR_CUDA;
   maps.k = maps.q;
   maps.v = maps.q;
-  maps.o = maps.q;  // unused: varlen rows are stored by the threads
+  // the epilogue's tile stores of full 128-row tiles (16-bit output): {d, T, H} over [T, H, d]
+  if (p.out_f32)
+    maps.o = maps.q;
+  else if (!make_rows_map(&maps.o, out, dtype, total_tokens, H, d, static_cast<long long>(H) * d, d))
+    return ATTN_ERR_CUDA;
   return from_cuda(attn::launch_fwd_tc(maps, p, dtype, causal != 0, attn::kModeVarlen, s));
 }
 

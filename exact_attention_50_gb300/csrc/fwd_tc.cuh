@@ -212,11 +212,16 @@ __global__ void __launch_bounds__(352, 1)
                   const FwdParams p, int n_items) {
   constexpr bool VARLEN = MODE == kModeVarlen;
   constexpr bool KV = MODE == kModeKv;
-  // Dense 16-bit output: the softmax warps stage each item's O tile in the item's Q slot (free
-  // once its last S has run) and warp 10 writes it with tile stores, then frees the slot.
-  // Otherwise (varlen rows must not spill into the next sequence; fp32 or KV-cache partials)
-  // the softmax warps store their rows themselves and the last S frees the Q slot.
-  const bool tile_epi = MODE == kModeDense && !p.out_f32;
+  // 16-bit output of a dense item, or of a varlen item whose 128 rows all lie in its
+  // sequence: the softmax warps stage the item's O tile in the item's Q slot (free once its
+  // last S has run) and warp 10 writes it with tile stores, then frees the slot.  Otherwise (a
+  // varlen tile that ends past its sequence must not write into the next one; fp32 output or
+  // KV-cache partials) the softmax warps store their rows themselves and the last S frees the
+  // Q slot.  Every role decides per item with the same function.
+  const bool tile_out = (MODE == kModeDense || MODE == kModeVarlen) && !p.out_f32;
+  auto tile_item = [&](const FwdItem& it) -> bool {
+    return tile_out && (MODE == kModeDense || (it.qt + 1) * kBM <= it.seq_len);
+  };
   using L = FwdLayout<DP>;
   constexpr int SQ = L::kStagesQ, SK = L::kStagesK, SV = L::kStagesV;
   constexpr int kChunks = DP / 64;
@@ -248,7 +253,7 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* o_free = pv_done + 2;
   uint64_t* xch = o_free + 1;       // [quadrant][slot]: row-max / row-sum exchange, warps q and q + 4
   uint64_t* drain = xch + 8;
-  uint64_t* o_staged = drain + 1;  // the softmax warps have written the item's O tile (tile_epi)
+  uint64_t* o_staged = drain + 1;  // the softmax warps have written a tile-stored item's O tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(352, 1)
             issue_s(ts, qs);
             mma_commit(k_empty + ts % SK);
             ++ns;
-            if (ns == n && !tile_epi) mma_commit(q_empty + qs);
+            if (ns == n && !tile_item(it)) mma_commit(q_empty + qs);
             progress = true;
           }
           const uint32_t tp = t0 + np;
@@ -487,20 +492,25 @@ __global__ void __launch_bounds__(352, 1)
     __syncwarp();
   } else if (warp == 10) {
     // ================================================================ output tile stores
-    if (lane == 0 && tile_epi) {
+    if (lane == 0 && tile_out) {
       tma_prefetch_desc(&tmO);
-      uint32_t ic = 0;
+      uint32_t ic = 0, nt = 0;  // items; items stored by tiles (o_staged phases)
       for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
         const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
         if (!it.valid) continue;
-        const uint32_t qs = ic % SQ;
-        if (!mbar_wait(o_staged, ic & 1, abort_flag, p.status)) break;
-        for (int c = 0; c < kChunks; ++c)
-          tma_store_3d(&tmO, sQ + qs * L::kTileBytes + c * L::kChunkBytes, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
+        const uint32_t qs = ic++ % SQ;
+        if (!tile_item(it)) continue;
+        if (!mbar_wait(o_staged, nt++ & 1, abort_flag, p.status)) break;
+        for (int c = 0; c < kChunks; ++c) {
+          const uint8_t* src = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
+          if constexpr (VARLEN)  // map {d, T, H} over the [T, H, d] output
+            tma_store_3d(&tmO, src, c * 64, it.seq_start + it.qt * kBM, it.h);
+          else
+            tma_store_3d(&tmO, src, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
+        }
         bulk_commit();
         bulk_wait_read<0>();
         mbar_arrive(q_empty + qs);  // the slot may take the Q of the item after next
-        ++ic;
       }
       bulk_wait_all();  // the stores are complete before the CTA ends
     }
@@ -677,7 +687,8 @@ __global__ void __launch_bounds__(352, 1)
       const bool o_f32 = KV || p.out_f32;
       void* const o_base = KV ? static_cast<void*>(p.o_part) : p.o;
       uint32_t r[32];
-      if (tile_epi) {
+      const bool tile = tile_item(it);
+      if (tile) {
         // this group's DP / 2 columns of row `row` (from column grp * DP / 2) into the item's Q
         // slot, in the 128-byte swizzled layout of the output map's {64, 128} boxes: column
         // col lands in box col / 64, 16-byte granule (col % 64) / 8; rows and columns past the
@@ -709,7 +720,7 @@ __global__ void __launch_bounds__(352, 1)
         mbar_arrive_warp(o_staged);
       }
 #pragma unroll
-      for (int c = 0; c < (tile_epi ? 0 : DP / 64); ++c) {
+      for (int c = 0; c < (tile ? 0 : DP / 64); ++c) {
         tmem_ld32(tO + c * 32, r);
         tmem_ld_wait();
         tmem_reg_fence(r);
@@ -740,7 +751,7 @@ __global__ void __launch_bounds__(352, 1)
           }
         }
       }
-      if (!tile_epi) {
+      if (!tile) {
         tc_fence_before();
         mbar_arrive_warp(o_free);
       }
