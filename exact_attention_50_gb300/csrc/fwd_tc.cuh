@@ -62,15 +62,18 @@ constexpr float kRescaleLog2 = 8.0f;
 // save (measured with 1/2, 1/4, 1/8 and none of the pairs on the FMA pipe: none is fastest).
 constexpr unsigned kPolyPairs = 0x00u;
 
-template <int DP>
+template <int DP, int MODE>
 struct FwdLayout {
   // For d = 128 two Q tiles, three K and two V tiles in flight (224 KB in all): an L2 load
   // takes up to ~3000 cycles when every SM streams K and V, about two tiles of work.  The
   // second Q slot lets the next item's Q load while the current item's slot, once its last S
   // has run, stages the item's output tile for the tile stores.  (1 Q + 3 V measured the same.)
-  static constexpr int kStagesQ = 2;
+  // The KV-cache mode stores no output tiles and streams K and V from HBM: one Q slot and a
+  // third V stage (more bytes in flight) serve it better.
+  static constexpr bool kKv = MODE == kModeKv;
+  static constexpr int kStagesQ = (DP == 128 && kKv) ? 1 : 2;
   static constexpr int kStagesK = DP == 128 ? 3 : 4;
-  static constexpr int kStagesV = DP == 128 ? 2 : 4;
+  static constexpr int kStagesV = DP == 128 ? (kKv ? 3 : 2) : 4;
   static constexpr int kChunkBytes = 128 * 128;          // 128 rows x 64 elements x 2 B
   static constexpr int kTileBytes = (DP / 64) * kChunkBytes;
   static constexpr int kOffQ = 0;
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(352, 1)
   auto tile_item = [&](const FwdItem& it) -> bool {
     return tile_out && (MODE == kModeDense || (it.qt + 1) * kBM <= it.seq_len);
   };
-  using L = FwdLayout<DP>;
+  using L = FwdLayout<DP, MODE>;
   constexpr int SQ = L::kStagesQ, SK = L::kStagesK, SV = L::kStagesV;
   constexpr int kChunks = DP / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -789,7 +792,7 @@ inline int sm_count() {
 
 template <typename T, int DP, bool CAUSAL, int MODE>
 cudaError_t launch_fwd_tc_t(const FwdMaps& maps, const FwdParams& p, cudaStream_t stream) {
-  using L = FwdLayout<DP>;
+  using L = FwdLayout<DP, MODE>;
   auto kern = fwd_tc_kernel<T, DP, CAUSAL, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
