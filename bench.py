@@ -163,7 +163,7 @@ class ClockSampler:
 
 def source_stamp() -> str:
     from exact_attention_50_gb300 import build
-    return build._stamp()
+    return build.code_stamp()
 
 
 def committed_traffic(kernel: str, workload: str):

@@ -41,6 +41,26 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
+def code_stamp() -> str:
+    """Hash of the compiled code alone: the CUDA sources and headers with comments and blank
+    lines removed (and the flags).  Profiles of a kernel stay valid while it is unchanged;
+    edits to comments do not change it."""
+    import re
+    h = hashlib.sha256()
+    h.update(" ".join(FLAGS).encode())
+    for d in (CSRC, INCLUDE):
+        for name in sorted(os.listdir(d)):
+            if name.endswith((".cu", ".cuh", ".h")):
+                with open(os.path.join(d, name)) as f:
+                    text = f.read()
+                text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+                text = re.sub(r"//[^\n]*", "", text)
+                lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+                h.update(name.encode())
+                h.update("\n".join(lines).encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile every translation unit and link the shared library; returns its path."""
     os.makedirs(BUILD_DIR, exist_ok=True)

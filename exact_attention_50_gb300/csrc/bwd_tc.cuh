@@ -23,8 +23,8 @@
 //   WG0, WG1  elementwise (two warps per TMEM lane quadrant, each on half of the 128 query
 //             columns): phase 1 turns S^T into P^T (hi/lo, back into TMEM), phase 2 turns dP^T
 //             into dS^T (hi/lo, into shared memory).  The next tile's LSE and D are prefetched.
-//   WG2       moves dQ_t from TMEM into the fp32 workspace (16-byte vector reductions) and
-//             writes dK, dV at the end.
+//   WG2       moves dQ_t from TMEM through shared memory into the fp32 workspace (TMA tile
+//             reductions; in key-tile order when deterministic) and writes dK, dV at the end.
 //   WG3       warp 12: TMA producer and TMEM allocator; warp 13: MMA issuer.
 // MMA order per query tile: S^T, dP^T, dV (hi, lo), dK (hi, lo), dQ (hi, lo).  The next
 // tile's S^T waits only for dV to have read P^T; its dP^T waits for the dQ readout.  Q and dO

@@ -5,20 +5,26 @@
 //   S_ij = scale * Q_i . K_j, masked to -inf for j > i (causal) and for keys past the sequence;
 //   online softmax over key tiles (running max m and sum l, exp2 with log2(e) folded into the
 //   scale); O_i = sum_j P_ij V_j / l_i; LSE_i = m_i + ln l_i.
+// In the KV-cache mode a row is query i = row % Nq of the G query heads of a kv head, its keys
+// are those of one range of the cache, masked past the cache length L and, when causal, past
+// L - Nq + i; it writes fp32 partials that a combine kernel merges.
 // The tiling follows the attention-operator article (m.xxqk.cn/news/636956) section 2.2: Q/K/V
 // tiles staged on chip, the max-subtracted softmax kept in registers and only O written back.
 // The online max/sum update follows the FlashAttention-T review, best practice 4; scale and
 // mask are applied inside the GEMM loop as in its best practice 2.
 //
-// A CTA loops over 128-row query tiles (heaviest first under the causal mask).  320 threads:
+// A CTA loops over 128-row query tiles (heaviest first under the causal mask).  352 threads:
 //   warps 0-3  softmax, key columns 0-63 of each S tile; warps 4-7 softmax, key columns 64-127.
 //              Thread t of either group owns query row t (TMEM lane t).  The two threads of a
 //              row exchange their partial row maxima through shared memory, so both use the
 //              same running max; each keeps its own partial row sum, combined at the end.  Each
 //              writes its 64 P values (16-bit pairs) into its 32 columns of the P buffer,
-//              rescales its half of the O row when the max moved, and writes that half of O.
+//              rescales its half of the O row when the max moved, and at the end normalises
+//              that half of O: into the item's Q slot for a tile store, or to global memory.
 //   warp 8     TMA producer (lane 0) and TMEM allocator (whole warp).
 //   warp 9     MMA issuer (lane 0): a non-blocking scheduler over the streams S(j) and PV(j).
+//   warp 10    output tile stores (lane 0): writes each staged O tile with TMA and frees the
+//              Q slot.
 // TMEM: S double buffer at columns [0,128) and [128,256), P double buffer (16-bit pairs) at
 // [256,320) and [320,384), O at [384, 384+DP).  S(j) goes into S buffer j % 2 as soon as the
 // softmax has loaded S(j-2) into registers, and P(j) into P buffer j % 2 once PV(j-2) has read
