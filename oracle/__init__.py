@@ -58,6 +58,7 @@ def _bind(lib):
                                        + [c_int] * 6 + [c_double])
     lib.oracle_fwd_varlen.argtypes = [_dp, _i32p, c_int, c_int, _dp, _dp, c_int, c_int, c_int, c_double]
     lib.oracle_fwd_kvcache.argtypes = [_dp, _dp, _dp, _i32p, _dp, _dp] + [c_int] * 7 + [c_double]
+    lib.oracle_bwd_cross.argtypes = [_dp] * 7 + [c_int] * 7 + [c_double]
     lib.oracle_num_threads.restype = c_int
     lib.oracle_set_num_threads.argtypes = [c_int]
     return lib
@@ -218,3 +219,20 @@ def fwd_kvcache(q, k, v, cache_seqlens, causal: bool, scale=None, lib=None):
     if rc:
         raise ValueError(f"oracle_fwd_kvcache rejected its arguments ({rc})")
     return o, lse
+
+
+def bwd_cross(q, k, v, dout, causal: bool, scale=None, lib=None):
+    """(dQ [B,Hq,Nq,d], dK, dV [B,Hkv,Nk,d]) of the cross-attention forward (fwd_kvcache with
+    full caches) for the upstream gradient dout [B,Hq,Nq,d]."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk_ = k.shape
+    if (Bk, dk_) != (B, d) or v.shape != k.shape or dout.shape != q.shape:
+        raise ValueError("q, k, v and dout shapes disagree")
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    lib = lib or _load()
+    rc = lib.oracle_bwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                              B, Hq, Hkv, Nq, Nk, d, int(causal), _scale(scale))
+    if rc:
+        raise ValueError(f"oracle_bwd_cross rejected its arguments ({rc})")
+    return dq, dk, dv

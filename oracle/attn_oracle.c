@@ -463,3 +463,79 @@ int oracle_fwd_kvcache(const double *q, const double *k, const double *v, const 
     }
     return err ? -2 : 0;
 }
+
+/* Backward of oracle_fwd_kvcache without cache lengths (cross-attention: Nq queries, Nk keys,
+ * every cache full), with its bottom-right causal alignment: query i sees key j iff
+ * j <= Nk - Nq + i when causal.  For an upstream gradient dout [B,Hq,Nq,d] it returns dq
+ * [B,Hq,Nq,d] and dk, dv [B,Hkv,Nk,d] from the same analytic formulas as oracle_bwd
+ * (dP_ij = dO_i . V_j, D_i = sum_j P_ij dP_ij, dS_ij = P_ij (dP_ij - D_i), dQ_i = sc sum_j
+ * dS_ij K_j, dK_j = sc sum_i dS_ij Q_i, dV_j = sum_i P_ij dO_i over the query heads of the
+ * group), written out per (batch, query head) with explicit P rows.  Rows that see no key
+ * (Nq > Nk under the causal mask) have P = 0 and contribute nothing. */
+int oracle_bwd_cross(const double *q, const double *k, const double *v, const double *dout, double *dq,
+                     double *dk, double *dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                     double scale) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0 || Hq % Hkv != 0) return -1;
+    if (!(scale >= 0.0)) return -1;
+    double sc = default_scale(scale, d);
+    int G = Hq / Hkv;
+    memset(dq, 0, sizeof(double) * (size_t)B * Hq * Nq * d);
+    memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+    memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+    int err = 0;
+    /* one (batch, kv head) per task: its dk, dv rows are written by that task alone */
+#pragma omp parallel
+    {
+        double *P = malloc(sizeof(double) * ((size_t)Nq * Nk + 1));
+        double *dS = malloc(sizeof(double) * ((size_t)Nq * Nk + 1));
+        if (!P || !dS) err = 1;
+#pragma omp for schedule(dynamic, 1)
+        for (long bg = 0; bg < (long)B * Hkv; ++bg) {
+            if (!P || !dS) continue;
+            int b = (int)(bg / Hkv), g = (int)(bg % Hkv);
+            const double *kb = k + bg * (long)Nk * d, *vb = v + bg * (long)Nk * d;
+            double *dkb = dk + bg * (long)Nk * d, *dvb = dv + bg * (long)Nk * d;
+            for (int h = g * G; h < (g + 1) * G; ++h) {
+                long qh = (long)b * Hq + h;
+                const double *qb = q + qh * Nq * d, *dob = dout + qh * Nq * d;
+                double *dqb = dq + qh * Nq * d;
+                for (int i = 0; i < Nq; ++i) {
+                    int last = causal ? Nk - Nq + i : Nk - 1;
+                    if (last > Nk - 1) last = Nk - 1;
+                    double *Pi = P + (long)i * Nk, *dSi = dS + (long)i * Nk;
+                    double m = -INFINITY;
+                    for (int j = 0; j < Nk; ++j) {
+                        if (j > last) { Pi[j] = -INFINITY; continue; }
+                        double acc = 0.0;
+                        for (int c = 0; c < d; ++c) acc += qb[(long)i * d + c] * kb[(long)j * d + c];
+                        Pi[j] = sc * acc;
+                        if (Pi[j] > m) m = Pi[j];
+                    }
+                    double l = 0.0;
+                    for (int j = 0; j <= last; ++j) l += exp(Pi[j] - m);
+                    for (int j = 0; j < Nk; ++j) Pi[j] = (j <= last) ? exp(Pi[j] - m) / l : 0.0;
+                    double Dv = 0.0;
+                    for (int j = 0; j < Nk; ++j) {
+                        double dp = 0.0;
+                        for (int c = 0; c < d; ++c) dp += dob[(long)i * d + c] * vb[(long)j * d + c];
+                        dSi[j] = dp;
+                        Dv += Pi[j] * dp;
+                    }
+                    for (int j = 0; j < Nk; ++j) dSi[j] = Pi[j] * (dSi[j] - Dv);
+                    for (int j = 0; j < Nk; ++j)
+                        for (int c = 0; c < d; ++c) dqb[(long)i * d + c] += sc * dSi[j] * kb[(long)j * d + c];
+                }
+                for (int j = 0; j < Nk; ++j)
+                    for (int i = 0; i < Nq; ++i) {
+                        double pij = P[(long)i * Nk + j], dsij = dS[(long)i * Nk + j];
+                        for (int c = 0; c < d; ++c) {
+                            dvb[(long)j * d + c] += pij * dob[(long)i * d + c];
+                            dkb[(long)j * d + c] += sc * dsij * qb[(long)i * d + c];
+                        }
+                    }
+            }
+        }
+        free(P); free(dS);
+    }
+    return err ? -2 : 0;
+}

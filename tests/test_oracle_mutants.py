@@ -32,6 +32,13 @@ MUTANTS = [
     ("kvcache ignores the cache length", "int L = lens ? lens[b] : Nk;", "int L = Nk;", None),
     ("kvcache GQA heads strided", "kvh = h / G;", "kvh = h % Hkv;", None),
     ("kvcache empty row LSE 0", "if (lse) lse[r] = -INFINITY;", "if (lse) lse[r] = 0.0;", None),
+    ("cross bwd causal mask top-left aligned", "int last = causal ? Nk - Nq + i : Nk - 1;",
+     "int last = causal ? i : Nk - 1;", None),
+    ("cross bwd drops D", "dSi[j] = Pi[j] * (dSi[j] - Dv);", "dSi[j] = Pi[j] * dSi[j];", None),
+    ("cross bwd dK misses the scale", "dkb[(long)j * d + c] += sc * dsij * qb[(long)i * d + c];",
+     "dkb[(long)j * d + c] += dsij * qb[(long)i * d + c];", None),
+    ("cross bwd dV from Q", "dvb[(long)j * d + c] += pij * dob[(long)i * d + c];",
+     "dvb[(long)j * d + c] += pij * qb[(long)i * d + c];", None),
     ("default scale is 1/d", "return scale == 0.0 ? 1.0 / sqrt((double)d) : scale;",
      "return scale == 0.0 ? 1.0 / (double)d : scale;", None),
 ]

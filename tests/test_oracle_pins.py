@@ -426,3 +426,66 @@ def test_kvcache_rejects_bad_lengths(lib=None):
     for lens in ([12, 1, 1], [-1, 2, 2]):
         with pytest.raises(ValueError):
             oracle.fwd_kvcache(q, k, v, lens, False, lib=lib)
+
+
+# ---------------------------------------------------------------- cross-attention backward
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(3, 5), (5, 3)])
+def test_cross_bwd_matches_central_differences(Nq, Nk, causal, lib=None):
+    """dQ, dK, dV against central differences (h = 1e-6) of L = sum(O * dO), O from the
+    KV-cache forward with full caches; with Nq > Nk under the causal mask the first rows see
+    no key (O = 0 there, no gradient)."""
+    rng = np.random.default_rng(40 + Nq)
+    B, Hq, Hkv, d = 1, 2, 1, 8
+    q, k, v = rand(rng, B, Hq, Nq, d), rand(rng, B, Hkv, Nk, d), rand(rng, B, Hkv, Nk, d)
+    dout = rand(rng, B, Hq, Nq, d)
+    grads = oracle.bwd_cross(q, k, v, dout, causal, lib=lib)
+    h = 1e-6
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.fwd_kvcache(qq, kk, vv, None, causal, lib=lib)
+        return float((o * dout).sum())
+
+    for which, (x, g) in enumerate(zip((q, k, v), grads)):
+        fd = np.empty_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p, args_m = [q, k, v], [q, k, v]
+            args_p[which], args_m[which] = xp, xm
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.linalg.norm(fd - g) / max(np.linalg.norm(g), 1e-300)
+        assert err <= 1e-7, (which, err)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_cross_bwd_matches_torch_lower_right_sdpa(causal, lib=None):
+    """torch's float64 SDPA with its bottom-right causal mask and autograd, GQA, Nq < Nk."""
+    rng = np.random.default_rng(45)
+    B, Hq, Hkv, Nq, Nk, d = 2, 4, 2, 6, 19, 16
+    q, k, v = rand(rng, B, Hq, Nq, d), rand(rng, B, Hkv, Nk, d), rand(rng, B, Hkv, Nk, d)
+    dout = rand(rng, B, Hq, Nq, d)
+    sc = 0.27
+    import warnings
+    from torch.nn.attention.bias import causal_lower_right
+    t = [torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v)]
+    with warnings.catch_warnings():
+        warnings.simplefilter("ignore")
+        mask = causal_lower_right(Nq, Nk)._materialize(device="cpu") if causal else None
+    o = F.scaled_dot_product_attention(t[0], t[1], t[2], attn_mask=mask, scale=sc, enable_gqa=True)
+    o.backward(torch.tensor(dout))
+    got = oracle.bwd_cross(q, k, v, dout, causal, scale=sc, lib=lib)
+    for g, x in zip(got, t):
+        np.testing.assert_allclose(g, x.grad.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_cross_bwd_square_is_dense_backward(causal, lib=None):
+    rng = np.random.default_rng(46)
+    q, k, v, dout = rand(rng, 1, 4, 11, 16), rand(rng, 1, 2, 11, 16), rand(rng, 1, 2, 11, 16), rand(rng, 1, 4, 11, 16)
+    for a, b in zip(oracle.bwd_cross(q, k, v, dout, causal, lib=lib), oracle.bwd(q, k, v, dout, causal, lib=lib)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
