@@ -67,6 +67,10 @@ def load() -> ctypes.CDLL:
         lib.attn_fwd_kvcache_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_fwd_kvcache.argtypes = [vp] * 7 + [ctypes.c_size_t] + [i] * 7 + [f, i, i, u, vp]
         lib.attn_fwd_kvcache.restype = i
+        lib.attn_bwd_cross_workspace_bytes.argtypes = [i, i, i, i, i, i, u]
+        lib.attn_bwd_cross_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_bwd_cross.argtypes = [vp] * 10 + [ctypes.c_size_t] + [i] * 7 + [f, i, u, vp]
+        lib.attn_bwd_cross.restype = i
         lib.attn_get_device_status.argtypes = [vp]
         lib.attn_get_device_status.restype = i
         lib.attn_status_string.argtypes = [i]
@@ -107,6 +111,16 @@ def attn_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, o, lse, workspace, work
                      causal, scale, num_splits, dtype, flags, stream) -> int:
     return load().attn_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, o, lse, workspace, workspace_bytes, B, Hq, Hkv,
                                    Nq, Nk, d, int(causal), float(scale), int(num_splits), dtype, flags, stream)
+
+
+def attn_bwd_cross_workspace_bytes(B, Hq, Nq, Nk, d, dtype, flags) -> int:
+    return load().attn_bwd_cross_workspace_bytes(B, Hq, Nq, Nk, d, dtype, flags)
+
+
+def attn_bwd_cross(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, Nq, Nk, d, causal,
+                   scale, dtype, flags, stream) -> int:
+    return load().attn_bwd_cross(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, Nq, Nk,
+                                 d, int(causal), float(scale), dtype, flags, stream)
 
 
 def attn_bwd_workspace_bytes(B, Hq, N, d) -> int:

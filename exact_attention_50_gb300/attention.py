@@ -104,6 +104,33 @@ def bwd(q, k, v, o, lse, dout, causal: bool, scale=None, out_f32: bool = False, 
     return dq, dk, dv
 
 
+def bwd_cross(q, k, v, o, lse, dout, causal: bool, scale=None, out_f32: bool = False, workspace=None,
+              deterministic: bool = False):
+    """Cross-attention backward (Nq <= Nk, bottom-right causal alignment).  q, o, dout
+    [B,Hq,Nq,d]; k, v [B,Hkv,Nk,d]; lse [B,Hq,Nq] from fwd_kvcache without cache lengths.
+    Returns (dq, dk, dv)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _require(t, n, q.dtype)
+    _require(lse, "lse", torch.float32)
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape or lse.shape != (B, Hq, Nq):
+        raise ValueError("o and dout must be shaped like q, v like k, lse [B,Hq,Nq]")
+    odt = torch.float32 if out_f32 else q.dtype
+    dq = torch.empty(q.shape, dtype=odt, device=q.device)
+    dk = torch.empty(k.shape, dtype=odt, device=q.device)
+    dv = torch.empty(v.shape, dtype=odt, device=q.device)
+    flags = _bwd_flags(out_f32, deterministic)
+    nbytes = _lib.attn_bwd_cross_workspace_bytes(B, Hq, Nq, Nk, d, _dtype_code(q), flags)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    st = _lib.attn_bwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                             B, Hq, Hkv, Nq, Nk, d, causal, _scale_arg(scale), _dtype_code(q), flags, _stream())
+    _lib._check(st, "attn_bwd_cross")
+    return dq, dk, dv
+
+
 def fwd_varlen(qkv, cu_seqlens, max_seqlen: int, causal: bool, scale=None, out_f32: bool = False,
                with_lse: bool = True):
     """Packed varlen forward.  qkv [T,3,H,d], cu_seqlens int32 [nseq+1] (device).
@@ -193,7 +220,12 @@ def fwd_kvcache(q, k_cache, v_cache, cache_seqlens=None, causal: bool = False, s
 class _AttnFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, causal, scale, deterministic):
-        o, lse = fwd(q, k, v, causal, scale)
+        # queries and keys of different lengths: cross-attention (bottom-right causal alignment)
+        ctx.cross = q.dim() == 4 and k.dim() == 4 and q.shape[2] != k.shape[2]
+        if ctx.cross:
+            o, lse = fwd_kvcache(q, k, v, None, causal, scale)
+        else:
+            o, lse = fwd(q, k, v, causal, scale)
         ctx.save_for_backward(q, k, v, o, lse)
         ctx.causal, ctx.scale, ctx.deterministic = causal, scale, deterministic
         return o
@@ -201,13 +233,15 @@ class _AttnFn(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dout):
         q, k, v, o, lse = ctx.saved_tensors
-        dq, dk, dv = bwd(q, k, v, o, lse, dout.contiguous(), ctx.causal, ctx.scale, deterministic=ctx.deterministic)
+        call = bwd_cross if ctx.cross else bwd
+        dq, dk, dv = call(q, k, v, o, lse, dout.contiguous(), ctx.causal, ctx.scale, deterministic=ctx.deterministic)
         return dq, dk, dv, None, None, None
 
 
 def flash_attention(q, k, v, causal: bool = True, scale=None, deterministic: bool = False):
-    """Exact attention of [B,Hq,N,d] queries over [B,Hkv,N,d] keys/values (Hq % Hkv == 0).
-    deterministic makes the backward's dq bitwise reproducible (slower)."""
+    """Exact attention of [B,Hq,Nq,d] queries over [B,Hkv,Nk,d] keys/values (Hq % Hkv == 0).
+    Nq != Nk is cross-attention, with the causal mask aligned to the last Nq keys (its backward
+    needs Nq <= Nk).  deterministic makes the backward's dq bitwise reproducible (slower)."""
     return _AttnFn.apply(q, k, v, causal, scale, bool(deterministic))
 
 

@@ -41,23 +41,41 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
-def code_stamp() -> str:
-    """Hash of the compiled code alone: the CUDA sources and headers with comments and blank
-    lines removed (and the flags).  Profiles of a kernel stay valid while it is unchanged;
-    edits to comments do not change it."""
+# Host-only sources: the C ABI entry points (argument checks, tensor maps, launches).  Their
+# device code is the status word alone; include/attn.h reaches the kernels only through the
+# ATTN_ status and flag constants.
+HOST_SOURCES = ("attn_api.cu",)
+
+
+def code_stamp(read=None) -> str:
+    """Hash of the device code: every CUDA source and header that holds kernels or device
+    functions, with comments and blank lines removed, the device declarations of the host-only
+    sources, the ATTN_ constants of the C header, and the flags.  Kernel profiles stay valid
+    while it is unchanged: edits to comments, to host-side entry points or to declarations do
+    not change it.  `read(path)` returns a file's text (default: the working tree)."""
     import re
+    read = read or (lambda path: open(path).read())
+
+    def strip(text):
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        return [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+
     h = hashlib.sha256()
     h.update(" ".join(FLAGS).encode())
-    for d in (CSRC, INCLUDE):
-        for name in sorted(os.listdir(d)):
-            if name.endswith((".cu", ".cuh", ".h")):
-                with open(os.path.join(d, name)) as f:
-                    text = f.read()
-                text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-                text = re.sub(r"//[^\n]*", "", text)
-                lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
-                h.update(name.encode())
-                h.update("\n".join(lines).encode())
+    for name in sorted(os.listdir(CSRC)):
+        if not name.endswith((".cu", ".cuh", ".h")):
+            continue
+        lines = strip(read(os.path.join(CSRC, name)))
+        if name in HOST_SOURCES:
+            lines = [ln for ln in lines if "__device__" in ln or "__global__" in ln]
+        h.update(name.encode())
+        h.update("\n".join(lines).encode())
+    for name in sorted(os.listdir(INCLUDE)):
+        if name.endswith(".h"):
+            lines = [ln for ln in strip(read(os.path.join(INCLUDE, name))) if re.search(r"\bATTN_\w+\s*(=|\d)", ln)]
+            h.update(name.encode())
+            h.update("\n".join(lines).encode())
     return h.hexdigest()
 
 

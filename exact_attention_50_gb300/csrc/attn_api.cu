@@ -320,6 +320,62 @@ size_t attn_bwd_varlen_workspace_bytes(int total_tokens, int H, int d) {
   return attn_bwd_workspace_bytes(1, H, total_tokens, d);
 }
 
+size_t attn_bwd_cross_workspace_bytes(int B, int Hq, int Nq, int Nk, int d, attn_dtype_t dtype, unsigned flags) {
+  if (B <= 0 || Hq <= 0 || Nq <= 0 || Nk < Nq || d <= 0) return 0;
+  const size_t bwd = attn_bwd_workspace_bytes(B, Hq, Nk, d);
+  if (Nq == Nk) return bwd;
+  const size_t es = dtype == ATTN_F32 ? 4 : 2;
+  const size_t eo = (dtype == ATTN_F32 || (flags & ATTN_FLAG_OUT_F32)) ? 4 : es;
+  const size_t rows = static_cast<size_t>(B) * Hq * Nk;
+  return bwd + 3 * round256(rows * d * es) + round256(rows * sizeof(float)) + round256(rows * d * eo);
+}
+
+// Cross-attention backward on the square kernels: with bottom-right alignment query i sees the
+// keys that row Nk - Nq + i of an Nk-query problem sees, so q, o, dout and lse are placed at
+// the end of Nk-row buffers whose leading rows are zero (dO = 0 and D = 0 there, so they add
+// nothing to dK and dV), attn_bwd runs on those, and dq is copied back out.
+attn_status_t attn_bwd_cross(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                             const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                             attn_dtype_t dtype, unsigned flags, void* stream) {
+  attn_status_t st = check_common(d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (B < 0 || Nq < 0 || Nk < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~(ATTN_FLAG_OUT_F32 | ATTN_FLAG_DETERMINISTIC)) return ATTN_ERR_INVALID_ARG;
+  if (Nq > Nk) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Nq == 0) return ATTN_OK;
+  if (!all_aligned16({q, k, v, o, dout, dq, dk, dv}) || !lse || !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < attn_bwd_cross_workspace_bytes(B, Hq, Nq, Nk, d, dtype, flags))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t bwd_bytes = attn_bwd_workspace_bytes(B, Hq, Nk, d);
+  if (Nq == Nk)
+    return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, bwd_bytes, B, Hq, Hkv, Nk, d, causal, scale,
+                    dtype, flags, stream);
+  const size_t es = dtype == ATTN_F32 ? 4 : 2;
+  const size_t eo = (dtype == ATTN_F32 || (flags & ATTN_FLAG_OUT_F32)) ? 4 : es;
+  const size_t heads = static_cast<size_t>(B) * Hq, rows = heads * Nk, pad = static_cast<size_t>(Nk - Nq);
+  char* qp = static_cast<char*>(workspace) + bwd_bytes;
+  char* op = qp + round256(rows * d * es);
+  char* dop = op + round256(rows * d * es);
+  char* lsep = dop + round256(rows * d * es);
+  char* dqp = lsep + round256(rows * sizeof(float));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto place = [&](char* dst, const void* src, size_t row_bytes) -> bool {
+    return cudaMemset2DAsync(dst, Nk * row_bytes, 0, pad * row_bytes, heads, s) == cudaSuccess &&
+           cudaMemcpy2DAsync(dst + pad * row_bytes, Nk * row_bytes, src, Nq * row_bytes, Nq * row_bytes, heads,
+                             cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+  };
+  if (!place(qp, q, d * es) || !place(op, o, d * es) || !place(dop, dout, d * es) ||
+      !place(lsep, lse, sizeof(float)))
+    return ATTN_ERR_CUDA;
+  st = attn_bwd(qp, k, v, op, dop, reinterpret_cast<const float*>(lsep), dqp, dk, dv, workspace, bwd_bytes, B, Hq,
+                Hkv, Nk, d, causal, scale, dtype, flags, stream);
+  if (st != ATTN_OK) return st;
+  return from_cuda(cudaMemcpy2DAsync(dq, Nq * d * eo, dqp + pad * d * eo, Nk * d * eo, Nq * d * eo, heads,
+                                     cudaMemcpyDeviceToDevice, s));
+}
+
 attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout, const float* lse,
                               const int32_t* cu_seqlens, int nseq, int total_tokens, int max_seqlen, void* dqkv,
                               void* workspace, size_t workspace_bytes, int H, int d, int causal, float scale,

@@ -162,6 +162,24 @@ attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout
                               attn_dtype_t dtype, unsigned flags, void* stream);
 
 /*
+ * Backward of cross-attention (the KV-cache forward above without cache lengths, Nq <= Nk),
+ * with the same bottom-right causal alignment: gradients of q [B,Hq,Nq,d] and of k, v
+ * [B,Hkv,Nk,d] for the forward's output o and LSE (natural log, [B,Hq,Nq]) and dL/do.
+ * Under that alignment query i sees exactly the keys that row Nk - Nq + i of an Nk-query
+ * problem sees, so the call runs attn_bwd on copies of q, o, dout and lse placed at the end of
+ * Nk-row buffers with zero leading rows (which add nothing), then copies dq out.
+ *   workspace  DEVICE, at least attn_bwd_cross_workspace_bytes(B, Hq, Nq, Nk, d, dtype, flags)
+ *              bytes, 256-byte aligned
+ * Nq > Nk returns ATTN_ERR_UNSUPPORTED; Nq == Nk is attn_bwd.  Flags, layouts and the other
+ * argument rules are those of attn_bwd.
+ */
+size_t attn_bwd_cross_workspace_bytes(int B, int Hq, int Nq, int Nk, int d, attn_dtype_t dtype, unsigned flags);
+attn_status_t attn_bwd_cross(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                             const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                             attn_dtype_t dtype, unsigned flags, void* stream);
+
+/*
  * KV cache / cross-attention forward: Nq queries per (batch, query head) against a cache of up to
  * Nk keys per (batch, kv head) (the FlashAttention-T review, FAQ 4: at inference the KV cache is
  * computed in blocks; its practical advice 2: the prefill and decode phases).  Decode is Nq = 1

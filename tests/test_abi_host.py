@@ -195,3 +195,31 @@ def test_kvcache_splits_workspace_and_validation(lib):
     assert f(d=40) == _lib.ATTN_ERR_UNSUPPORTED
     assert f(flags=2) == _lib.ATTN_ERR_INVALID_ARG
     assert f(scale=-1.0) == _lib.ATTN_ERR_INVALID_ARG
+
+
+def test_bwd_cross_workspace_and_validation(lib):
+    W = _lib.attn_bwd_cross_workspace_bytes
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert W(2, 4, 100, 100, 64, _lib.ATTN_BF16, 0) == _lib.attn_bwd_workspace_bytes(2, 4, 100, 64)
+    rows = 2 * 4 * 300
+    assert W(2, 4, 100, 300, 64, _lib.ATTN_BF16, 0) == (_lib.attn_bwd_workspace_bytes(2, 4, 300, 64)
+                                                       + 3 * r256(rows * 64 * 2) + r256(rows * 4) + r256(rows * 64 * 2))
+    assert W(2, 4, 100, 300, 64, _lib.ATTN_BF16, _lib.ATTN_FLAG_OUT_F32) == (
+        _lib.attn_bwd_workspace_bytes(2, 4, 300, 64) + 3 * r256(rows * 64 * 2) + r256(rows * 4) + r256(rows * 64 * 4))
+    assert W(2, 4, 301, 300, 64, _lib.ATTN_BF16, 0) == 0  # Nq > Nk is not provided
+    ws = W(2, 4, 100, 300, 64, _lib.ATTN_BF16, 0)
+
+    def f(**kw):
+        a = dict(p=4096, lse=4096, ws=4096, wsb=ws, B=2, Hq=4, Hkv=2, Nq=100, Nk=300, d=64, flags=0)
+        a.update(kw)
+        return _lib.attn_bwd_cross(a["p"], a["p"], a["p"], a["p"], a["p"], a["lse"], a["p"], a["p"], a["p"], a["ws"],
+                                   a["wsb"], a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["d"], 1, 0.0,
+                                   _lib.ATTN_BF16, a["flags"], None)
+    assert f(Nq=301) == _lib.ATTN_ERR_UNSUPPORTED
+    assert f(B=0) == _lib.ATTN_OK and f(Nq=0) == _lib.ATTN_OK
+    assert f(p=4100) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(lse=None) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(wsb=ws - 1) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(ws=4096 + 128) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(Hq=3) == _lib.ATTN_ERR_INVALID_ARG
+    assert f(flags=4) == _lib.ATTN_ERR_INVALID_ARG
