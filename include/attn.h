@@ -219,7 +219,7 @@ attn_status_t attn_fwd_kvcache(const void* q, const void* k_cache, const void* v
  *     from any allocator).  Every GPU that loads the library holds that array until the process
  *     exits.  No call on this path allocates or frees device memory.
  *   - Sizes are limited by it: when attn_bwd_workspace_bytes(B, Hq, N, d) exceeds 64 MiB
- *     (67108864 bytes; at d = 128 that is about 127,000 query rows B*Hq*N) the call returns
+ *     (67108864 bytes; at d = 128 that is about 129,000 query rows B*Hq*N) the call returns
  *     ATTN_ERR_UNSUPPORTED and launches nothing.
  *   - The first call on each device looks up the array's device address (a one-time set-up on
  *     that device, made while it is current); make that first call before any stream capture.
