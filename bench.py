@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded CPU-baseline sample time")
     ap.add_argument("--deterministic", action="store_true", help="backward with bitwise reproducible dQ")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other configurations timed after the default workload")
     return ap.parse_args(argv)
 
 
@@ -93,17 +95,6 @@ def read_peaks():
     out = dict(FALLBACK_PEAKS)
     out["source"] = "fallback"
     return out
-
-
-def workload_flops(wl, lengths=None):
-    from exact_attention_50_gb300 import workloads as W
-    if "Nq" in wl.extra:  # KV cache: forward only, over the keys each query sees
-        return W.kvcache_fwd_flops(lengths, wl.Hq, wl.extra["Nq"], wl.d, wl.causal), 0.0
-    if wl.varlen:
-        f = W.varlen_fwd_flops(lengths, wl.Hq, wl.d, wl.causal)
-        return f, (2.5 * f if wl.backward else 0.0)
-    f = W.fwd_flops(wl.B, wl.Hq, wl.N, wl.d, wl.causal)
-    return f, (W.bwd_flops(wl.B, wl.Hq, wl.N, wl.d, wl.causal) if wl.backward else 0.0)
 
 
 class ClockSampler:
@@ -269,6 +260,222 @@ def oracle_sample(wl, seconds: float, seed: int = 0):
 
 # ------------------------------------------------------------------ our arm
 
+class Step:
+    """The launches of one step of a workload through the C ABI, with its inputs resident on
+    the device, and what the measurement needs to know about them."""
+
+    def __init__(self):
+        self.calls = []          # [(name, fn)] in launch order; fn returns an attn status
+        self.kernels = 0         # kernels launched per step
+        self.fwd_f = self.bwd_f = 0.0
+        self.host_in, self.dev_in, self.dev_out = [], [], []
+        self.lengths = None
+        self.kv_bytes = None     # decode: algorithmic HBM bytes per step
+        self.nsplit = None
+        self.dom = None          # (kernel name, index of its call, its algorithmic FLOPs or bytes)
+
+
+def setup_step(wl, dev, lib, sp, bwd_flags) -> Step:
+    import torch
+    from exact_attention_50_gb300 import workloads as W
+    S = Step()
+    dt_code = {"f32": 0, "f16": 1, "bf16": 2}[wl.dtype]
+    scale = 0.0 if wl.scale is None else float(wl.scale)
+    if "Nq" in wl.extra:
+        Nq = wl.extra["Nq"]
+        q_h, k_h, v_h, cl_h = W.kvcache_inputs(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, wl.dtype, wl.extra["lens"],
+                                               seed=0)
+        S.lengths = cl_h.tolist()
+        q, k, v, cl = q_h.to(dev), k_h.to(dev), v_h.to(dev), cl_h.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(wl.B, wl.Hq, Nq, dtype=torch.float32, device=dev)
+        S.nsplit = lib.attn_fwd_kvcache_splits(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, 0)
+        nbytes = lib.attn_fwd_kvcache_workspace_bytes(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, 0)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        # a step serves one new token per sequence: its query in, its output out; the caches
+        # stay resident (in the end-to-end leg too: they are the state a decoder keeps)
+        S.host_in, S.dev_in, S.dev_out = [q_h], [q], [o]
+        # algorithmic HBM bytes: the K and V rows of each (batch, kv head) that its queries see,
+        # read once, plus Q read and O and LSE written (the split partials are not counted)
+        rows = wl.B * wl.Hq * Nq
+        S.kv_bytes = (sum(S.lengths) * wl.Hkv * wl.d * 2 * q_h.element_size() + 2 * rows * wl.d * q_h.element_size()
+                      + rows * 4)
+        S.calls = [("fwd_kvcache", lambda: lib.attn_fwd_kvcache(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), cl.data_ptr(), o.data_ptr(), lse.data_ptr(), ws.data_ptr(),
+            nbytes, wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, int(wl.causal), scale, 0, dt_code, 0, sp))]
+        S.kernels = 2  # the forward kernel and the split combine
+        S.fwd_f = W.kvcache_fwd_flops(S.lengths, wl.Hq, Nq, wl.d, wl.causal)
+        S.dom = ("fwd_tc_kernel + kv_combine_kernel", 0, S.kv_bytes)
+        return S
+    if wl.varlen:
+        qkv_h, cu_h, lengths, _ = W.varlen_inputs(wl.varlen, wl.Hq, wl.d, wl.dtype, seed=0)
+        S.lengths = lengths
+        T = qkv_h.shape[0]
+        qkv, cu = qkv_h.to(dev), cu_h.to(dev)
+        out = torch.empty(T, wl.Hq, wl.d, dtype=qkv.dtype, device=dev)
+        lse = torch.empty(wl.Hq, T, dtype=torch.float32, device=dev)
+        maxlen = max(lengths)
+        S.host_in, S.dev_in, S.dev_out = [qkv_h], [qkv], [out]
+        S.calls = [("fwd_varlen", lambda: lib.attn_fwd_varlen(
+            qkv.data_ptr(), cu.data_ptr(), len(lengths), T, maxlen, out.data_ptr(), lse.data_ptr(), wl.Hq, wl.d,
+            int(wl.causal), scale, dt_code, 0, sp))]
+        S.kernels = 1
+        S.fwd_f = W.varlen_fwd_flops(lengths, wl.Hq, wl.d, wl.causal)
+        S.dom = ("fwd_tc_kernel", 0, S.fwd_f)
+        if wl.backward:
+            g = torch.Generator().manual_seed(1)
+            do_h = torch.randn(T, wl.Hq, wl.d, generator=g).to(qkv_h.dtype)
+            dout = do_h.to(dev)
+            dqkv = torch.empty_like(qkv)
+            nbytes = lib.attn_bwd_varlen_workspace_bytes(T, wl.Hq, wl.d)
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            S.host_in.append(do_h)
+            S.dev_in.append(dout)
+            S.dev_out.append(dqkv)
+            S.calls.append(("bwd_varlen", lambda: lib.attn_bwd_varlen(
+                qkv.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(), cu.data_ptr(), len(lengths), T,
+                maxlen, dqkv.data_ptr(), ws.data_ptr(), nbytes, wl.Hq, wl.d, int(wl.causal), scale, dt_code,
+                bwd_flags, sp)))
+            S.kernels += 3
+            S.bwd_f = 2.5 * S.fwd_f
+            # one call: its prepare and finish steps are inside the time
+            S.dom = ("bwd_tc_kernel", 1, S.bwd_f)
+        return S
+    q_h, k_h, v_h, do_h = W.dense_inputs(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.dtype, seed=0, with_dout=wl.backward)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(wl.B, wl.Hq, wl.N, dtype=torch.float32, device=dev)
+    S.host_in, S.dev_in, S.dev_out = [q_h, k_h, v_h], [q, k, v], [o]
+    dims = (wl.B, wl.Hq, wl.Hkv, wl.N, wl.d)
+    S.calls = [("fwd", lambda: lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                             *dims, int(wl.causal), scale, dt_code, 0, sp))]
+    S.kernels = 1
+    S.fwd_f = W.fwd_flops(wl.B, wl.Hq, wl.N, wl.d, wl.causal)
+    S.dom = ("fwd_f32_kernel" if wl.dtype == "f32" else "fwd_tc_kernel", 0, S.fwd_f)
+    if wl.backward:
+        dout = do_h.to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        nbytes = lib.attn_bwd_workspace_bytes(wl.B, wl.Hq, wl.N, wl.d)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        S.host_in.append(do_h)
+        S.dev_in.append(dout)
+        S.dev_out += [dq, dk, dv]
+        S.calls += [
+            ("bwd_prepare", lambda: lib.attn_bwd_prepare(o.data_ptr(), dout.data_ptr(), ws.data_ptr(), nbytes, wl.B,
+                                                         wl.Hq, wl.N, wl.d, dt_code, sp)),
+            ("bwd_main", lambda: lib.attn_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                                                   lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                                   ws.data_ptr(), nbytes, *dims, int(wl.causal), scale, dt_code,
+                                                   bwd_flags, sp)),
+            ("bwd_finish", lambda: lib.attn_bwd_finish(dq.data_ptr(), ws.data_ptr(), nbytes, wl.B, wl.Hq, wl.N, wl.d,
+                                                       scale, dt_code, 0, sp)),
+        ]
+        S.kernels += 3
+        S.bwd_f = W.bwd_flops(wl.B, wl.Hq, wl.N, wl.d, wl.causal)
+        S.dom = ("bwd_tc_kernel", 2, S.bwd_f)
+    return S
+
+
+def run_step(S, stream, evs=None):
+    from exact_attention_50_gb300 import _lib
+    for i, (name, c) in enumerate(S.calls):
+        if evs is not None:
+            evs[i].record(stream)
+        st = c()
+        if st != 0:
+            raise RuntimeError(f"{name} failed: {_lib.status_string(st)}")
+    if evs is not None:
+        evs[len(S.calls)].record(stream)
+
+
+def time_steps(S, stream, K, sampler=None, barrier=lambda: None):
+    """K steps bracketed by a barrier and a device synchronisation on both sides, timed with
+    CUDA events on the launching stream; returns (total ms, mean ms of each call)."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(S.calls) + 1)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        run_step(S, stream, evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler is not None else None
+    barrier()
+    per_call = [statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                for j in range(len(S.calls))]
+    return t0.elapsed_time(t1), per_call, clocks
+
+
+def choose_peak(peaks, clocks, region_s: float):
+    """The dense bf16 denominator for a region: the sustained (power-capped) figure only when
+    the clock record shows the power cap during a region of at least a second, else the burst
+    figure of a short run at full clock."""
+    capped = bool(clocks) and "sw_power_cap" in clocks.get("reasons", [])
+    if capped and region_s >= 1.0:
+        return peaks["bf16_tflops_sustained"], "sustained", \
+            f"sw_power_cap seen during a {region_s:.2f} s timed region"
+    why = "no power cap in the clock record" if not capped else f"timed region only {region_s:.3f} s"
+    return peaks["bf16_tflops"], "burst", f"{why}; {region_s:.3f} s timed region"
+
+
+def fp32_alu_peak(sm_count: int, sm_mhz: float) -> float:
+    """fp32 CUDA-core peak in TFLOP/s: SMs x 128 fp32 lanes x 2 FLOPs per FMA x SM clock."""
+    return sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+# Configurations timed after the main workload, each on its own (a few steps, inputs resident):
+# the forward-only configurations, the varlen forward, the long-context step and the fp32
+# CUDA-core forward at a size that is not launch-bound.
+EXTRA_WORKLOADS = ("mha_f16", "mha_f16_causal", "varlen_bf16", "long_bf16", "f32_bh256")
+
+
+def time_extra(name, dev, lib, stream, sp, peaks, sm_count, sm_mhz, budget_s=0.4):
+    import torch
+    from exact_attention_50_gb300 import workloads as W
+    wl = W.WORKLOADS[name]
+    S = setup_step(wl, dev, lib, sp, 0)
+    for _ in range(3):
+        run_step(S, stream)
+    ms1, _, _ = time_steps(S, stream, 1)
+    K = int(max(3, min(50, budget_s * 1e3 / max(ms1, 1e-3))))
+    ms, per_call, _ = time_steps(S, stream, K)
+    st = lib.attn_get_device_status(sp)
+    if st != 0:
+        raise RuntimeError(f"device status after {name}: {st}")
+    ent = {"workload": wl.name, "steps": K, "ms_per_step": ms / K}
+    burst = peaks["bf16_tflops"]
+    names = [n for n, _ in S.calls]
+    if wl.dtype == "f32":
+        peak = fp32_alu_peak(sm_count, sm_mhz)
+        tf = S.fwd_f / (per_call[0] * 1e-3) / 1e12
+        ent.update({"fwd_ms": per_call[0], "fwd_tflops": tf,
+                    "roofline": {"kernel": "fwd_f32_kernel", "bound": "alu", "achieved": tf, "peak": peak,
+                                 "unit": "TFLOP/s", "frac": tf / peak,
+                                 "peak_source": f"derived: {sm_count} SMs x 128 fp32 lanes x 2 FLOP/FMA x "
+                                                f"{sm_mhz:.0f} MHz"}})
+        return ent
+    tf = S.fwd_f / (per_call[0] * 1e-3) / 1e12
+    ent.update({"fwd_ms": per_call[0], "fwd_tflops": tf, "fwd_frac_burst": tf / burst})
+    if "bwd_main" in names:
+        i = names.index("bwd_main")
+        bwd_ms = sum(per_call[1:])
+        main_tf = S.bwd_f / (per_call[i] * 1e-3) / 1e12
+        ent.update({"bwd_ms": bwd_ms, "bwd_tflops": S.bwd_f / (bwd_ms * 1e-3) / 1e12,
+                    "bwd_frac_burst": S.bwd_f / (bwd_ms * 1e-3) / 1e12 / burst,
+                    "bwd_main_ms": per_call[i], "bwd_main_tflops": main_tf, "bwd_main_frac_burst": main_tf / burst,
+                    "step_tflops": (S.fwd_f + S.bwd_f) / (ms / K * 1e-3) / 1e12})
+    if S.lengths is not None and wl.varlen:
+        ent["total_tokens"] = sum(S.lengths)
+    del S
+    torch.cuda.empty_cache()
+    return ent
+
+
 def run_ours(args, rank, world, local):
     import torch
     import torch.distributed as dist
@@ -282,124 +489,17 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
-    dt_code = {"f32": _lib.ATTN_F32, "f16": _lib.ATTN_F16, "bf16": _lib.ATTN_BF16}[wl.dtype]
-    scale = 0.0 if wl.scale is None else float(wl.scale)
     bwd_flags = _lib.ATTN_FLAG_DETERMINISTIC if args.deterministic else 0
-
-    lengths = None
-    kv_bytes = None
-    if "Nq" in wl.extra:
-        Nq = wl.extra["Nq"]
-        q_h, k_h, v_h, cl_h = W.kvcache_inputs(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, wl.dtype, wl.extra["lens"],
-                                               seed=0)
-        lengths = cl_h.tolist()
-        q, k, v, cl = q_h.to(dev), k_h.to(dev), v_h.to(dev), cl_h.to(dev)
-        o = torch.empty_like(q)
-        lse = torch.empty(wl.B, wl.Hq, Nq, dtype=torch.float32, device=dev)
-        nsplit = lib.attn_fwd_kvcache_splits(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, 0)
-        nbytes = lib.attn_fwd_kvcache_workspace_bytes(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, 0)
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        # a step serves one new token per sequence: its query in, its output out; the caches
-        # stay resident (in the end-to-end leg too: they are the state a decoder keeps)
-        host_in = [q_h]
-        dev_in = [q]
-        dev_out = [o]
-        # algorithmic HBM bytes: the K and V rows of each (batch, kv head) that its queries see,
-        # read once, plus Q read and O and LSE written (the split partials are not counted)
-        rows = wl.B * wl.Hq * Nq
-        kv_bytes = (sum(lengths) * wl.Hkv * wl.d * 2 * q_h.element_size() + 2 * rows * wl.d * q_h.element_size()
-                    + rows * 4)
-
-        def fwd_call():
-            return lib.attn_fwd_kvcache(q.data_ptr(), k.data_ptr(), v.data_ptr(), cl.data_ptr(), o.data_ptr(),
-                                        lse.data_ptr(), ws.data_ptr(), nbytes, wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d,
-                                        int(wl.causal), scale, 0, dt_code, 0, sp)
-        bwd_calls = []
-    elif wl.varlen:
-        qkv_h, cu_h, lengths, _ = W.varlen_inputs(wl.varlen, wl.Hq, wl.d, wl.dtype, seed=0)
-        T = qkv_h.shape[0]
-        qkv = qkv_h.to(dev)
-        cu = cu_h.to(dev)
-        out = torch.empty(T, wl.Hq, wl.d, dtype=qkv.dtype, device=dev)
-        lse = torch.empty(wl.Hq, T, dtype=torch.float32, device=dev)
-        maxlen = max(lengths)
-        host_in = [qkv_h]
-        dev_in = [qkv]
-        dev_out = [out]
-
-        def fwd_call():
-            return lib.attn_fwd_varlen(qkv.data_ptr(), cu.data_ptr(), len(lengths), T, maxlen, out.data_ptr(),
-                                       lse.data_ptr(), wl.Hq, wl.d, int(wl.causal), scale, dt_code, 0, sp)
-        bwd_calls = []
-        if wl.backward:
-            g = torch.Generator().manual_seed(1)
-            do_h = torch.randn(T, wl.Hq, wl.d, generator=g).to(qkv_h.dtype)
-            dout = do_h.to(dev)
-            dqkv = torch.empty_like(qkv)
-            nbytes = lib.attn_bwd_varlen_workspace_bytes(T, wl.Hq, wl.d)
-            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-            host_in.append(do_h)
-            dev_in.append(dout)
-            dev_out.append(dqkv)
-            bwd_calls = [
-                lambda: lib.attn_bwd_varlen(qkv.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-                                            cu.data_ptr(), len(lengths), T, maxlen, dqkv.data_ptr(), ws.data_ptr(),
-                                            nbytes, wl.Hq, wl.d, int(wl.causal), scale, dt_code, bwd_flags, sp),
-            ]
-    else:
-        q_h, k_h, v_h, do_h = W.dense_inputs(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.dtype, seed=0,
-                                             with_dout=wl.backward)
-        q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
-        o = torch.empty_like(q)
-        lse = torch.empty(wl.B, wl.Hq, wl.N, dtype=torch.float32, device=dev)
-        host_in = [q_h, k_h, v_h]
-        dev_in = [q, k, v]
-        dev_out = [o]
-        args_dims = (wl.B, wl.Hq, wl.Hkv, wl.N, wl.d)
-
-        def fwd_call():
-            return lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), *args_dims,
-                                int(wl.causal), scale, dt_code, 0, sp)
-        bwd_calls = []
-        if wl.backward:
-            dout = do_h.to(dev)
-            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-            nbytes = lib.attn_bwd_workspace_bytes(wl.B, wl.Hq, wl.N, wl.d)
-            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-            host_in.append(do_h)
-            dev_in.append(dout)
-            dev_out += [dq, dk, dv]
-            bwd_calls = [
-                lambda: lib.attn_bwd_prepare(o.data_ptr(), dout.data_ptr(), ws.data_ptr(), nbytes, wl.B, wl.Hq,
-                                             wl.N, wl.d, dt_code, sp),
-                lambda: lib.attn_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-                                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), nbytes,
-                                          *args_dims, int(wl.causal), scale, dt_code, bwd_flags, sp),
-                lambda: lib.attn_bwd_finish(dq.data_ptr(), ws.data_ptr(), nbytes, wl.B, wl.Hq, wl.N, wl.d, scale,
-                                            dt_code, 0, sp),
-            ]
-    calls = [fwd_call] + bwd_calls
-    launches_per_step = len(calls)
-    kernels_per_step = launches_per_step + (1 if kv_bytes is not None else 0)  # + the split combine
-    fwd_f, bwd_f = workload_flops(wl, lengths)
-    step_flops = fwd_f + bwd_f
-
-    def run_step(evs=None):
-        for i, c in enumerate(calls):
-            if evs is not None:
-                evs[i].record(stream)
-            st = c()
-            if st != 0:
-                raise RuntimeError(f"call {i} failed: {_lib.status_string(st)}")
-        if evs is not None:
-            evs[len(calls)].record(stream)
+    S = setup_step(wl, dev, lib, sp, bwd_flags)
+    step_flops = S.fwd_f + S.bwd_f
+    kernels_per_step, lengths, nsplit = S.kernels, S.lengths, S.nsplit
 
     def barrier():
         if world > 1:
             dist.barrier()
 
     for _ in range(max(args.warmup, 3)):
-        run_step()
+        run_step(S, stream)
     torch.cuda.synchronize()
     st = lib.attn_get_device_status(sp)
     if st != 0:
@@ -407,31 +507,16 @@ def run_ours(args, rank, world, local):
 
     # device-resident timed region (inputs larger than L2 for the default workload)
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(launches_per_step + 1)] for _ in range(K)]
     gpu_id = "0"
+    props = torch.cuda.get_device_properties(dev)
     try:
-        props = torch.cuda.get_device_properties(dev)
         uuid = str(getattr(props, "uuid", ""))
         if uuid:
             gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
     except Exception:
         pass
-    sampler = ClockSampler(gpu_id)
-    barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(K):
-        run_step(evs[i])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    barrier()
-    ms_total = t_start.elapsed_time(t_end)
-    per_call_ms = [statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
-                   for j in range(launches_per_step)]
+    ms_total, per_call_ms, clocks = time_steps(S, stream, K, ClockSampler(gpu_id), barrier)
+    region_s = ms_total * 1e-3
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
     st = lib.attn_get_device_status(sp)
@@ -442,26 +527,25 @@ def run_ours(args, rank, world, local):
     # end to end: pinned host inputs in, results out, inside the timed region
     e2e = None
     if not args.no_e2e:
-        hin = [t.pin_memory() for t in host_in]
-        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
+        hin = [t.pin_memory() for t in S.host_in]
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in S.dev_out]
         Ke = args.e2e_steps or max(3, min(K, 50))
-        for _ in range(2):
-            for h, d_ in zip(hin, dev_in):
+
+        def e2e_step():
+            for h, d_ in zip(hin, S.dev_in):
                 d_.copy_(h, non_blocking=True)
-            run_step()
-            for h, d_ in zip(hout, dev_out):
+            run_step(S, stream)
+            for h, d_ in zip(hout, S.dev_out):
                 h.copy_(d_, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
         torch.cuda.synchronize()
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(Ke):
-            for h, d_ in zip(hin, dev_in):
-                d_.copy_(h, non_blocking=True)
-            run_step()
-            for h, d_ in zip(hout, dev_out):
-                h.copy_(d_, non_blocking=True)
+            e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -472,41 +556,59 @@ def run_ours(args, rank, world, local):
                "ms_per_step": ms_e / Ke, "steps": Ke}
 
     peaks = read_peaks()
-    # dominant kernel: the backward main kernel when there is a backward, else the forward
-    if len(bwd_calls) == 3:
-        dom_name, dom_ms, dom_flops = "bwd_tc_kernel", per_call_ms[2], bwd_f
-    elif bwd_calls:  # one call (varlen): its prepare and finish steps are inside the time
-        dom_name, dom_ms, dom_flops = "bwd_tc_kernel", per_call_ms[1], bwd_f
-    else:
-        dom_name, dom_ms, dom_flops = "fwd_tc_kernel", per_call_ms[0], fwd_f
-    peak = peaks["bf16_tflops_sustained"] if wl.dtype != "f32" else None
-    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    traffic = committed_traffic(dom_name, args.workload)
-    roofline = {"kernel": dom_name, "bound": "tensor", "achieved": round(achieved, 2),
-                "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4) if peak else None,
-                "traffic": traffic, "peak_source": f"{peaks['source']} bf16 dense, sustained"}
+    sm_count = props.multi_processor_count
+    sm_mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    peak, peak_kind, peak_why = choose_peak(peaks, clocks, region_s)
+    burst = peaks["bf16_tflops"]
+    dom_name, dom_i, dom_work = S.dom
+    dom_ms = per_call_ms[dom_i]
+    kv_bytes = S.kv_bytes
     if kv_bytes is not None:
         # decode streams the caches once: HBM-bound; the call's time covers the forward kernel
         # and the split combine
-        gbs = kv_bytes / (per_call_ms[0] * 1e-3) / 1e9
+        gbs = kv_bytes / (dom_ms * 1e-3) / 1e9
         hbm = peaks.get("hbm_gbs")
-        roofline = {"kernel": "fwd_tc_kernel + kv_combine_kernel", "bound": "hbm", "achieved": round(gbs, 1),
-                    "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4) if hbm else None,
+        roofline = {"kernel": dom_name, "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(gbs / hbm, 4) if hbm else None,
                     "traffic": committed_traffic("fwd_tc_kernel", args.workload),
                     "algorithmic_bytes": int(kv_bytes), "peak_source": f"{peaks['source']} HBM copy"}
+    elif wl.dtype == "f32":
+        achieved = dom_work / (dom_ms * 1e-3) / 1e12
+        alu = fp32_alu_peak(sm_count, sm_mhz)
+        roofline = {"kernel": dom_name, "bound": "alu", "achieved": round(achieved, 3), "peak": round(alu, 2),
+                    "unit": "TFLOP/s", "frac": round(achieved / alu, 4), "traffic": None,
+                    "peak_source": f"derived: {sm_count} SMs x 128 fp32 lanes x 2 FLOP/FMA x {sm_mhz:.0f} MHz"}
+    else:
+        achieved = dom_work / (dom_ms * 1e-3) / 1e12
+        roofline = {"kernel": dom_name, "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "frac_burst": round(achieved / burst, 4),
+                    "frac_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                    "traffic": committed_traffic(dom_name, args.workload),
+                    "peak_source": f"{peaks['source']} bf16 dense, {peak_kind} ({peak_why})"}
     fwd_ms = per_call_ms[0]
-    detail = {"fwd_ms": fwd_ms, "fwd_tflops": fwd_f / (fwd_ms * 1e-3) / 1e12,
-              "fwd_frac": (fwd_f / (fwd_ms * 1e-3) / 1e12) / peak if peak else None}
-    if bwd_calls:
+    fwd_tf = S.fwd_f / (fwd_ms * 1e-3) / 1e12
+    detail = {"fwd_ms": fwd_ms, "fwd_tflops": fwd_tf}
+    if wl.dtype != "f32":
+        detail.update({"fwd_frac": fwd_tf / peak, "fwd_frac_burst": fwd_tf / burst, "peak_kind": peak_kind})
+    names = [n for n, _ in S.calls]
+    if len(names) > 1:
         bwd_ms = sum(per_call_ms[1:])
-        detail.update({"bwd_ms": bwd_ms, "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12,
-                       "bwd_frac": (bwd_f / (bwd_ms * 1e-3) / 1e12) / peak if peak else None})
-        if len(bwd_calls) == 3:
-            detail["bwd_phase_ms"] = {"prepare": per_call_ms[1], "main": per_call_ms[2], "finish": per_call_ms[3]}
+        bwd_tf = S.bwd_f / (bwd_ms * 1e-3) / 1e12
+        detail.update({"bwd_ms": bwd_ms, "bwd_tflops": bwd_tf, "bwd_frac": bwd_tf / peak,
+                       "bwd_frac_burst": bwd_tf / burst})
+        if "bwd_main" in names:
+            detail["bwd_phase_ms"] = {n.split("_", 1)[1]: per_call_ms[i] for i, n in enumerate(names) if i > 0}
+            main_tf = S.bwd_f / (per_call_ms[names.index("bwd_main")] * 1e-3) / 1e12
+            detail.update({"bwd_main_tflops": main_tf, "bwd_main_frac": main_tf / peak,
+                           "bwd_main_frac_burst": main_tf / burst})
 
     line = None
     if rank == 0:
+        if world == 1 and not args.no_extra and args.workload == "gqa_bf16":
+            del S
+            torch.cuda.empty_cache()
+            detail["configs"] = {n: time_extra(n, dev, lib, stream, sp, peaks, sm_count, sm_mhz)
+                                 for n in EXTRA_WORKLOADS}
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             v_, cores, sample = oracle_sample(wl, args.cpu_seconds)
@@ -514,18 +616,17 @@ def run_ours(args, rank, world, local):
         cfg = {"workload": wl.name, "global_batch": wl.B * world if not wl.varlen else len(lengths) * world,
                "seq_len": wl.N if not wl.varlen else max(lengths), "heads_q": wl.Hq, "heads_kv": wl.Hkv,
                "head_dim": wl.d, "causal": wl.causal, "parallelism": f"replicas x{world}",
-               "l2": "inputs larger than L2 (no flush)" if not wl.varlen else "inputs larger than L2 (no flush)",
-               "step": "fwd + bwd (prepare, main, finish)" if bwd_calls else "fwd"}
+               "l2": "inputs larger than L2 (no flush)",
+               "step": "fwd + bwd (prepare, main, finish)" if len(names) > 1 else "fwd"}
         if args.deterministic:
             cfg["deterministic"] = True
         if wl.varlen:
             cfg["total_tokens"] = sum(lengths)
-        if kv_bytes is not None:
+        if "Nq" in wl.extra:
             cfg.update({"queries_per_sequence": wl.extra["Nq"], "cache_capacity": wl.N,
-                        "cache_tokens": sum(lengths), "num_splits": nsplit,
-                        "step": "one decode forward (forward kernel + split combine)"})
-        line = {"metric": "attention TFLOP/s (fwd+bwd)" if bwd_calls else "attention TFLOP/s (fwd)",
-                "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+                        "cache_tokens": sum(lengths), "num_splits": nsplit, "step": "one decode forward (forward kernel + split combine)"})
+        metric = "attention TFLOP/s (fwd+bwd)" if len(names) > 1 else "attention TFLOP/s (fwd)"
+        line = {"metric": metric, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
                 "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,1))",
                 "config": cfg, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,

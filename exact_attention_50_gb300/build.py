@@ -47,6 +47,12 @@ def _stamp() -> str:
 HOST_SOURCES = ("attn_api.cu",)
 
 
+def _portable_flags() -> list:
+    """The compile flags without the include directories, which name absolute paths of the
+    checkout: the same sources compiled in another directory give the same stamp."""
+    return [f for f in FLAGS if not f.startswith("-I")]
+
+
 def code_stamp(read=None) -> str:
     """Hash of the device code: every CUDA source and header that holds kernels or device
     functions, with comments and blank lines removed, the device declarations of the host-only
@@ -62,7 +68,7 @@ def code_stamp(read=None) -> str:
         return [ln.rstrip() for ln in text.splitlines() if ln.strip()]
 
     h = hashlib.sha256()
-    h.update(" ".join(FLAGS).encode())
+    h.update(" ".join(_portable_flags()).encode())
     for name in sorted(os.listdir(CSRC)):
         if not name.endswith((".cu", ".cuh", ".h")):
             continue

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <initializer_list>
 #include <mutex>
 #include "kernels.h"
@@ -33,6 +34,23 @@ unsigned* status_word() {
     cache[dev] = static_cast<unsigned*>(ptr);
   }
   return cache[dev];
+}
+
+// The limit of any single device-side wait, in ns: ATTN_WAIT_LIMIT_MS from the environment when
+// the first call is made (10 .. 600000 ms), else 4 s.  A pipeline wait or a deterministic
+// backward's turn wait that exceeds it stops its CTA and reports ATTN_ERR_TIMEOUT.
+unsigned long long wait_limit_ns() {
+  static unsigned long long ns = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    ns = 4000000000ull;
+    if (const char* e = std::getenv("ATTN_WAIT_LIMIT_MS")) {
+      char* end = nullptr;
+      const long ms = std::strtol(e, &end, 10);
+      if (end != e && *end == '\0' && ms >= 10 && ms <= 600000) ns = static_cast<unsigned long long>(ms) * 1000000ull;
+    }
+  });
+  return ns;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -143,6 +161,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.o = o;
   p.lse = lse;
   p.status = status_word();
+  p.wait_ns = wait_limit_ns();
   if (!p.status) return ATTN_ERR_CUDA;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.G = Hq / Hkv;
   p.n_qtiles = n_qtiles;
@@ -186,6 +205,7 @@ attn_status_t attn_fwd_varlen(const void* qkv, const int32_t* cu_seqlens, int ns
   p.lse = lse;
   p.cu_seqlens = cu_seqlens;
   p.status = status_word();
+  p.wait_ns = wait_limit_ns();
   if (!p.status) return ATTN_ERR_CUDA;
   p.B = 1; p.Hq = H; p.Hkv = H; p.N = 0; p.d = d; p.G = 1;
   p.nseq = nseq; p.total_tokens = total_tokens; p.max_seqlen = max_seqlen;
@@ -236,6 +256,7 @@ attn_status_t bwd_setup(BwdParams* p, void* workspace, size_t workspace_bytes, i
   p->delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(rows * d * sizeof(float)));
   p->dq_turn = reinterpret_cast<int*>(reinterpret_cast<char*>(p->delta) + round256(rows * sizeof(float)));
   p->deterministic = (flags & ATTN_FLAG_DETERMINISTIC) ? 1 : 0;
+  p->wait_ns = wait_limit_ns();
   p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->N = N; p->d = d; p->G = Hq / Hkv;
   p->n_ktiles = (N + attn::kBN - 1) / attn::kBN;
   const BwdParams::Rows dense{d, static_cast<long long>(N) * d};
@@ -501,6 +522,7 @@ attn_status_t attn_fwd_kvcache(const void* q, const void* k_cache, const void* v
   p.o = o;
   p.lse = lse;
   p.status = status_word();
+  p.wait_ns = wait_limit_ns();
   if (!p.status) return ATTN_ERR_CUDA;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = Nk; p.d = d; p.G = G;
   p.Nq = Nq; p.Nk = Nk; p.R = static_cast<int>(R);

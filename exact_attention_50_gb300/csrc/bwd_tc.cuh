@@ -56,7 +56,7 @@ struct BwdLayout {
   // dv_done, ds_full, dsl_free, stage_free, dq_full, dq_free, dkdv_done, rows_ready,
   // stage_full, drain
   static constexpr int kNumBars = 1 + 4 * kQStages + 13;
-  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag, wait limit (u64)
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
   static_assert(kSmemAlloc <= 227 * 1024, "shared memory over the per-CTA limit");
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(stage_full, 4);
     mbar_init(drain, 1);
     abort_set(abort_flag, 0);
+    wait_limit_set(abort_flag, p.wait_ns);
     mbar_init_fence();
   }
   if (warp == 12) tmem_alloc(tmem_slot, L::kTmemCols);

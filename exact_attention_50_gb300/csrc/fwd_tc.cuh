@@ -90,7 +90,8 @@ struct FwdLayout {
   // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
   // s_free[2], p_full[2], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain, o_staged
   static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1 + 1;
-  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base (u32), abort flag (int)
+  // tmem base (u32), abort flag (int), wait limit (u64, ns)
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
   static constexpr uint32_t kTmemCols = 512;
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(drain, 1);
     mbar_init(o_staged, 8);
     abort_set(abort_flag, 0);
+    wait_limit_set(abort_flag, p.wait_ns);
     mbar_init_fence();
   }
   if (warp == 8) tmem_alloc(tmem_slot, L::kTmemCols);
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(352, 1)
           const unsigned long long now = globaltimer();
           if (t_idle == 0) t_idle = now;
           if (abort_read(abort_flag)) { ok = false; break; }
-          if (now - t_idle > kWaitTimeoutNs) {
+          if (now - t_idle > wait_limit(abort_flag)) {
             raise_status(p.status, ATTN_ERR_TIMEOUT);
             abort_set(abort_flag, 1);
             ok = false;
@@ -481,7 +483,7 @@ __global__ void __launch_bounds__(352, 1)
             const unsigned long long now = globaltimer();
             if (t_idle == 0) t_idle = now;
             if (abort_read(abort_flag)) { ok = false; break; }
-            if (now - t_idle > kWaitTimeoutNs) {
+            if (now - t_idle > wait_limit(abort_flag)) {
               raise_status(p.status, ATTN_ERR_TIMEOUT);
               abort_set(abort_flag, 1);
               ok = false;

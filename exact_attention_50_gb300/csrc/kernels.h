@@ -22,6 +22,7 @@ struct FwdParams {
   float scale;             // softmax scale (natural units)
   float scale_log2;        // scale * log2(e)
   int out_f32;             // write o as float32
+  unsigned long long wait_ns;  // limit of any single pipeline wait (0: the 4 s default)
   // KV cache / cross-attention: q [B,Hq,Nq,d] read as [B*Hkv, R = G*Nq, d] (the G query heads
   // of a kv head are consecutive), k and v [B,Hkv,Nk,d], cache_seqlens [B] (null: Nk each).
   // The key tiles of a (batch, kv head) are cut into n_splits ranges of tiles_per_split tiles;
@@ -83,6 +84,7 @@ struct BwdParams {
                    // 128-row dQ tile, the key tiles that have added into that tile
   int deterministic;  // add dQ tiles in key-tile order (ATTN_FLAG_DETERMINISTIC)
   unsigned* status;
+  unsigned long long wait_ns;  // limit of any single pipeline wait (0: the 4 s default)
   int B, Hq, Hkv, N, d, G;
   int n_ktiles;
   float scale, scale_log2;

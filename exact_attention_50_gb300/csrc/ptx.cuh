@@ -1,9 +1,10 @@
 // ptx.cuh -- hand-written inline PTX for sm_103a: mbarriers, TMA tile loads, tcgen05 (TMEM
 // allocation, MMA, commit, loads/stores) and the shared-memory / instruction descriptors.
 //
-// Every wait on an mbarrier is bounded: after kWaitTimeoutNs of %globaltimer time it records
-// ATTN_ERR_TIMEOUT in the device status word, raises the CTA's abort flag and returns false,
-// so a broken pipeline ends with an error status instead of a hung GPU.
+// Every wait on an mbarrier is bounded: after the CTA's wait limit (kWaitTimeoutNs unless the
+// launch sets another) of %globaltimer time it records ATTN_ERR_TIMEOUT in the device status
+// word, raises the CTA's abort flag and returns false, so a broken pipeline ends with an error
+// status instead of a hung GPU.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -11,7 +12,7 @@
 
 namespace attn {
 
-constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;  // 4 s per single wait
+constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;  // default: 4 s per single wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -65,6 +66,17 @@ __device__ __forceinline__ void abort_set(uint32_t flag, int v) {
   asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(flag), "r"(v) : "memory");
 }
 
+// The CTA's wait limit in ns: a 64-bit word in shared memory 4 bytes after the abort flag
+// (8-byte aligned), written once at the start of the kernel.
+__device__ __forceinline__ void wait_limit_set(uint32_t flag, unsigned long long ns) {
+  asm volatile("st.shared.u64 [%0], %1;" ::"r"(flag + 4), "l"(ns ? ns : kWaitTimeoutNs) : "memory");
+}
+__device__ __forceinline__ unsigned long long wait_limit(uint32_t flag) {
+  unsigned long long ns;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(ns) : "r"(flag + 4) : "memory");
+  return ns;
+}
+
 // Non-blocking probe: has the phase with the given parity completed?
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -88,7 +100,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     if (mbar_try_wait(b, parity)) return true;
     if ((it & 63u) == 0u) {
       if (abort_read(abort_flag)) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
+      if (globaltimer() - t0 > wait_limit(abort_flag)) {
         raise_status(status, ATTN_ERR_TIMEOUT);
         abort_set(abort_flag, 1);
         return false;
@@ -192,7 +204,7 @@ __device__ __forceinline__ bool wait_turn(const int* p, int target, uint32_t abo
     __nanosleep(100);
     if (ld_acquire_gpu(p) >= target) return true;
     if (abort_read(abort_flag)) return false;
-    if (globaltimer() - t0 > kWaitTimeoutNs) {
+    if (globaltimer() - t0 > wait_limit(abort_flag)) {
       raise_status(status, ATTN_ERR_TIMEOUT);
       abort_set(abort_flag, 1);
       return false;

@@ -46,6 +46,10 @@ class Workload:
 WORKLOADS = {
     "tiny_f32": Workload("tiny_f32 B1 H2 N128 d64 fp32 fwd", "f32", B=1, Hq=2, Hkv=2, N=128, d=64,
                          causal=False, scale=1.0 / 8.0, backward=False),
+    # the fp32 configuration's shape at B * H = 256: enough work for the CUDA-core kernel not to be
+    # launch-bound
+    "f32_bh256": Workload("f32_bh256 B128 H2 N128 d64 fp32 fwd", "f32", B=128, Hq=2, Hkv=2, N=128, d=64,
+                          causal=False, scale=1.0 / 8.0, backward=False),
     "mha_f16": Workload("mha_f16 B1 H32 N2048 d64 fp16 fwd", "f16", B=1, Hq=32, Hkv=32, N=2048,
                         d=64, causal=False, scale=1.0 / 8.0, backward=False),
     "mha_f16_causal": Workload("mha_f16_causal B1 H32 N2048 d64 fp16 causal fwd", "f16", B=1,

@@ -26,7 +26,10 @@
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream).  Argument errors are returned before anything is launched.
  *   - Errors found on the device (a pipeline wait that timed out, invalid cu_seqlens) are
- *     recorded in a per-device status word and returned by attn_get_device_status().
+ *     recorded in a per-device status word and returned by attn_get_device_status().  Every
+ *     device-side wait is bounded: 4 s by default, or ATTN_WAIT_LIMIT_MS milliseconds (10 to
+ *     600000) from the environment as read at the library's first call.  A CTA whose wait runs
+ *     out stops and reports ATTN_ERR_TIMEOUT; the CUDA context stays usable.
  *   - scale == 0 selects the default 1/sqrt(d); a negative or NaN scale is rejected.
  *   - d must be a multiple of 16 in [16, 128]; Hq must be a multiple of Hkv; query head h uses
  *     kv head h / (Hq / Hkv).
@@ -67,7 +70,13 @@ typedef enum {
 #define ATTN_FLAG_DETERMINISTIC 2u
 
 /*
- * Forward.
+ * Forward: O = softmax(scale * Q K^T, causally masked) V for every (batch, query head), tiled so
+ * the N x N scores stay on chip.  Defining passages: the attention-operator article
+ * (m.xxqk.cn/news/636956) section 2.1 (S = Q K^T, softmax, P V) and section 2.2 (the tiled form
+ * that writes only O back); the Aule-Attention summary (jeff.news/article/688), API list (layout
+ * [batch, heads, seq_len, head_dim], causal, default scale 1/sqrt(head_dim), head_dim <= 128,
+ * GQA); the FlashAttention-T review, best practice 4 (running max and sum, kept so the
+ * normalisation can be restored: the LSE below).
  *   q    [B, Hq,  N, d]   k, v [B, Hkv, N, d]   (dtype)
  *   o    [B, Hq,  N, d]   (dtype, or float32 with ATTN_FLAG_OUT_F32)
  *   lse  [B, Hq,  N] float32, nullable: natural-log log-sum-exp of the scaled, masked scores
@@ -80,7 +89,10 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        void* stream);
 
 /*
- * Forward on packed variable-length sequences (flash_attn_varlen_qkvpacked_func semantics).
+ * Forward on packed variable-length sequences (flash_attn_varlen_qkvpacked_func semantics:
+ * Turing varlen article (ewbang.com/community/article/details/1000323363), the function's
+ * argument list and its pseudo-code, which runs every sequence of cu_seqlens as its own
+ * attention problem and returns the packed [total_tokens, heads, head_dim] output).
  *   qkv         [total_tokens, 3, H, d] (dtype): plane 0 = q, 1 = k, 2 = v
  *   cu_seqlens  DEVICE int32 [nseq + 1]: 0-based prefix sums, cu_seqlens[nseq] == total_tokens;
  *               sequence s is tokens [cu_seqlens[s], cu_seqlens[s+1]); indices (and the causal
@@ -103,7 +115,12 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int d);
 
 /*
  * Backward: given dout = dL/dO, writes dq [B,Hq,N,d], dk and dv [B,Hkv,N,d] (dtype, or float32
- * with ATTN_FLAG_OUT_F32).  q, k, v, o are the forward's inputs and output and lse its
+ * with ATTN_FLAG_OUT_F32).  Defining passages: the Aule-Attention article (jdon.com/83460),
+ * the training example (loss.backward() through flash_attention gives the gradients of q, k
+ * and v); the FlashAttention-T review, FAQ 4 (the backward recomputes the score matrix from
+ * Q, K and the saved normalisation instead of storing it).  With P_ij = exp(S_ij - LSE_i),
+ * D_i = dO_i . O_i and dS_ij = P_ij (dO_i . V_j - D_i): dV_j = sum_i P_ij dO_i,
+ * dK_j = scale sum_i dS_ij Q_i, dQ_i = scale sum_j dS_ij K_j.  q, k, v, o are the forward's inputs and output and lse its
  * float32 LSE; P is recomputed from q, k and lse (nothing of size N x N is stored).  dk and
  * dv of a kv head sum the contributions of every query head of its group.
  *   workspace  DEVICE, at least attn_bwd_workspace_bytes(B, Hq, N, d) bytes, 256-byte aligned;
@@ -226,6 +243,9 @@ attn_status_t attn_fwd_kvcache(const void* q, const void* k_cache, const void* v
  *   - All calls share the one array and it keeps the last call's contents; each call clears the
  *     part that must start at zero itself.  Calls whose execution overlaps on the GPU (other
  *     streams, or other host threads) race on the array and give wrong results: order them.
+ *   - The cached address belongs to the device's primary context (the one the CUDA runtime
+ *     uses).  Do not call it from a different driver context, and not after cudaDeviceReset
+ *     in the same process: the address would no longer be valid there.
  */
 attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                                const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,

@@ -49,3 +49,23 @@ def test_replica_throughput_is_whole_job():
     import bench
     assert bench.replica_throughput(1e12, 4, 1000.0) == pytest.approx(4.0)
     assert bench.max_over_ranks(3.0, 1) == 3.0
+
+
+def test_peak_choice_follows_the_clock_record():
+    """A short region at full clock divides by the burst figure; the sustained one applies only
+    when the power cap was seen during a region of at least a second."""
+    import bench
+    peaks = {"bf16_tflops": 1915.3, "bf16_tflops_sustained": 1713.1}
+    free = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    capped = {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert bench.choose_peak(peaks, free, 0.014)[:2] == (1915.3, "burst")
+    assert bench.choose_peak(peaks, free, 5.0)[:2] == (1915.3, "burst")
+    assert bench.choose_peak(peaks, capped, 0.2)[:2] == (1915.3, "burst")
+    assert bench.choose_peak(peaks, capped, 3.0)[:2] == (1713.1, "sustained")
+    assert bench.choose_peak(peaks, None, 3.0)[:2] == (1915.3, "burst")
+
+
+def test_fp32_alu_peak_derivation():
+    import bench
+    # 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz
+    assert bench.fp32_alu_peak(152, 2070.0) == pytest.approx(80.55, rel=1e-3)

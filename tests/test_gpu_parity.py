@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle, element by element,
 on seeded inputs.  Small ragged shapes span several tiles and a partial tail; the full-size
-workloads are checked in the launch configuration the benchmark times, on everything the
-oracle finishes in seconds (one batch, a subset of sequences, sampled rows/keys) plus
-properties that hold at any size."""
+workloads are checked in the launch configuration the benchmark times: whole batches, whole kv
+groups and every varlen sequence element by element, plus sampled rows and keys of the parts
+the oracle would take minutes over."""
 import numpy as np
 import pytest
 import torch
@@ -153,7 +153,8 @@ def test_gqa_bf16_workload_full(dev):
     o_r, l_r = oracle.fwd_rows(to_np(q), to_np(k), to_np(v), rows, True)
     o_g = to_np(res["o32"])[rows[:, 0], rows[:, 1], rows[:, 2]]
     assert_close_f32(o_g, o_r, torch.bfloat16, "gqa_bf16 batch3 O rows")
-    keys = np.stack([np.full(8, 3), rng.integers(0, wl.Hkv, 8), rng.integers(wl.N - 300, wl.N, 8)], 1)
+    keys = np.stack([np.full(8, 3), rng.integers(0, wl.Hkv, 8), rng.integers(0, wl.N, 8)], 1)
+    keys[:3, 2] = [0, 127, wl.N - 1]
     dq_r, dk_r, dv_r = oracle.bwd_sampled(to_np(q), to_np(k), to_np(v), to_np(dout), rows[:16], keys, True)
     dq32, dk32, dv32 = (to_np(x) for x in res["g32"])
     assert_close_f32(dq32[rows[:16, 0], rows[:16, 1], rows[:16, 2]], dq_r, torch.bfloat16, "batch3 dQ rows")
@@ -161,50 +162,52 @@ def test_gqa_bf16_workload_full(dev):
     assert_close_f32(dv32[keys[:, 0], keys[:, 1], keys[:, 2]], dv_r, torch.bfloat16, "batch3 dV keys")
 
 
-def test_long_context_bf16_workload_sampled(dev):
-    """B=1, Hq=32, Hkv=8, N=32768, d=128 bf16 causal fwd+bwd at full size: sampled output rows
-    and LSE, sampled dQ rows, dK/dV of keys in the last tiles (whose causal dependents are few),
-    and for every kv head sum_j dK_j = 0 and sum_j dV_j = sum of the group's dO rows."""
+def test_long_context_bf16_workload_full_groups(dev):
+    """B=1, Hq=32, Hkv=8, N=32768, d=128 bf16 causal fwd+bwd, launched at full size.  KV groups
+    0 and 7 (their four query heads and one kv head each) are compared with the oracle element
+    by element in full: O and LSE of all 4 x 32768 rows, dQ of those rows, dK and dV of all
+    32768 keys, at the bf16 tolerance on the fp32 results and tol + half an ulp on the stored
+    bf16 ones.  The other groups get sampled rows and keys spread over the whole sequence."""
     wl = W.WORKLOADS["long_bf16"]
     q, k, v, dout = W.dense_inputs(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, "bf16", seed=0)
     res = gpu_fwd_bwd(q, k, v, dout, True, None, dev)
     G = wl.Hq // wl.Hkv
-    rng = np.random.default_rng(5)
     for g in (0, wl.Hkv - 1):
         hs = slice(g * G, (g + 1) * G)
+        sub = {"o32": res["o32"][:, hs], "o": res["o"][:, hs], "lse": res["lse"][:, hs],
+               "lse_n": res["lse_n"][:, hs],
+               "g32": (res["g32"][0][:, hs], res["g32"][1][:, g:g + 1], res["g32"][2][:, g:g + 1]),
+               "g": (res["g"][0][:, hs], res["g"][1][:, g:g + 1], res["g"][2][:, g:g + 1])}
+        check_dense(sub, q[:, hs], k[:, g:g + 1], v[:, g:g + 1], dout[:, hs], True, None, torch.bfloat16,
+                    f"long_bf16 group {g}")
+    # the other groups: rows and keys from the first tiles, the last ones and random places
+    rng = np.random.default_rng(5)
+    for g in range(1, wl.Hkv - 1):
+        hs = slice(g * G, (g + 1) * G)
         qs, ks, vs, ds = (to_np(t) for t in (q[:, hs], k[:, g:g + 1], v[:, g:g + 1], dout[:, hs]))
-        rows = np.stack([np.zeros(24, int), rng.integers(0, G, 24), rng.integers(0, wl.N, 24)], 1)
-        rows[:3, 2] = [0, 127, wl.N - 1]
+        rows = np.stack([np.zeros(12, int), rng.integers(0, G, 12), rng.integers(0, wl.N, 12)], 1)
+        rows[:4, 2] = [0, 1, 127, wl.N - 1]
+        keys = np.stack([np.zeros(8, int), np.zeros(8, int), rng.integers(0, wl.N, 8)], 1)
+        keys[:4, 2] = [0, 1, 127, wl.N - 1]
         o_r, l_r = oracle.fwd_rows(qs, ks, vs, rows, True)
+        dq_r, dk_r, dv_r = oracle.bwd_sampled(qs, ks, vs, ds, rows, keys, True)
         o_g = to_np(res["o32"][:, hs])[rows[:, 0], rows[:, 1], rows[:, 2]]
         l_g = to_np(res["lse"][:, hs])[rows[:, 0], rows[:, 1], rows[:, 2]]
+        dq_g = to_np(res["g32"][0][:, hs])[rows[:, 0], rows[:, 1], rows[:, 2]]
+        dk_g = to_np(res["g32"][1][:, g:g + 1])[0, 0, keys[:, 2]]
+        dv_g = to_np(res["g32"][2][:, g:g + 1])[0, 0, keys[:, 2]]
         assert_close_f32(o_g, o_r, torch.bfloat16, f"long O rows g={g}")
         assert_close_f32(l_g, l_r, torch.float16, f"long LSE rows g={g}")
-        keys = np.stack([np.zeros(6, int), np.zeros(6, int), wl.N - 1 - rng.integers(0, 200, 6)], 1)
-        dq_r, dk_r, dv_r = oracle.bwd_sampled(qs, ks, vs, ds, rows[:8], keys, True)
-        dq32 = to_np(res["g32"][0][:, hs])
-        dk32 = to_np(res["g32"][1][:, g:g + 1])
-        dv32 = to_np(res["g32"][2][:, g:g + 1])
-        assert_close_f32(dq32[rows[:8, 0], rows[:8, 1], rows[:8, 2]], dq_r, torch.bfloat16, f"long dQ g={g}")
-        assert_close_f32(dk32[0, 0, keys[:, 2]], dk_r, torch.bfloat16, f"long dK g={g}")
-        assert_close_f32(dv32[0, 0, keys[:, 2]], dv_r, torch.bfloat16, f"long dV g={g}")
-    # Properties over all 32768 keys.  Rounding leaves sum_j dK_j a small fraction of the
-    # size a sum of unrelated terms would have (sqrt(sum_j dK_j^2)); without the property the
-    # ratio would be of order 1.  Likewise sum_j dV_j against the sum of dO rows.
-    dk32 = res["g32"][1].double().cpu()
-    dv32 = res["g32"][2].double().cpu()
-    ratio = dk32.sum(dim=2).abs() / dk32.pow(2).sum(dim=2).sqrt()
-    assert float(ratio.max()) < 0.1, float(ratio.max())
-    expect = dout.double().reshape(1, wl.Hkv, G, wl.N, wl.d).sum(dim=(2, 3))
-    rel = (dv32.sum(dim=2) - expect).abs().max() / expect.abs().max()
-    assert float(rel) < 1e-2, float(rel)
+        assert_close_f32(dq_g, dq_r, torch.bfloat16, f"long dQ rows g={g}")
+        assert_close_f32(dk_g, dk_r, torch.bfloat16, f"long dK keys g={g}")
+        assert_close_f32(dv_g, dv_r, torch.bfloat16, f"long dV keys g={g}")
 
 
 # ------------------------------------------------------------------ varlen
 
 def test_varlen_bf16_workload(dev):
     """16 sequences, lengths ~ U[64, 4096] (seed 0), qkv [T,3,16,128], causal: every sequence's
-    rows are bit-identical to a dense forward of that sequence alone; three sequences are also
+    rows are bit-identical to a dense forward of that sequence alone, and every sequence is
     compared with the oracle element by element."""
     wl = W.WORKLOADS["varlen_bf16"]
     qkv, cu, lengths, _ = W.varlen_inputs(wl.varlen, wl.Hq, wl.d, "bf16", seed=0)
@@ -223,13 +226,12 @@ def test_varlen_bf16_workload(dev):
         assert torch.equal(out[a:b], o_n[0].transpose(0, 1)), f"sequence {s}: native rows differ"
         assert torch.equal(lse[:, a:b], l[0]), f"sequence {s}: LSE differs"
     status_ok()
-    order = np.argsort(lengths)
-    for s in (int(order[0]), int(order[1]), int(order[8])):
+    o_r, l_r = oracle.fwd_varlen(to_np(qkv), cu.numpy(), True)
+    for s in range(len(lengths)):
         a, b = cu_l[s], cu_l[s + 1]
-        o_r, l_r = oracle.fwd_varlen(to_np(qkv[a:b]), [0, b - a], True)
-        assert_close_f32(out32[a:b], o_r, torch.bfloat16, f"varlen seq {s} O")
-        assert_close_native(out[a:b], o_r, torch.bfloat16, f"varlen seq {s} O native")
-        assert_close_f32(lse[:, a:b], l_r, torch.float16, f"varlen seq {s} LSE")
+        assert_close_f32(out32[a:b], o_r[a:b], torch.bfloat16, f"varlen seq {s} O")
+        assert_close_native(out[a:b], o_r[a:b], torch.bfloat16, f"varlen seq {s} O native")
+        assert_close_f32(lse[:, a:b], l_r[:, a:b], torch.float16, f"varlen seq {s} LSE")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
