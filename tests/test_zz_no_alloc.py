@@ -30,19 +30,8 @@ def _fwd(q, k, v, causal, dtype_code, stream):
     return o, lse
 
 
-def _grads(q, k, v):
-    return torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-
-
-def _within_one_ulp(a, r, dtype):
-    """|a - r| <= one ulp of the storage dtype at max(|a|, |r|): the two runs add the same dQ
-    contributions in fp32, possibly in another order, before one rounding to dtype."""
-    a64, r64 = a.double(), r.double()
-    eps = {torch.bfloat16: 2.0 ** -7, torch.float16: 2.0 ** -10}[a.dtype]
-    mag = torch.maximum(a64.abs(), r64.abs())
-    _, e = torch.frexp(mag)
-    ulp = eps * torch.ldexp(torch.ones_like(mag), (e - 1).to(torch.int32))
-    return bool(((a64 - r64).abs() <= ulp + 1e-30).all())
+def _grads(q, k, v, dtype):
+    return tuple(torch.empty(t.shape, dtype=dtype, device=t.device) for t in (q, k, v))
 
 
 @pytest.mark.parametrize("dtype,causal,deterministic", [("bf16", True, False), ("f16", False, False),
@@ -50,25 +39,28 @@ def _within_one_ulp(a, r, dtype):
 def test_noalloc_backward_matches_workspace_backward_twice(dev, dtype, causal, deterministic):
     """Same kernels on the same inputs as attn_bwd: dK and dV bitwise equal on both calls; dQ
     bitwise equal in the deterministic mode (whose per-tile turn counters live in the shared
-    scratch array and must be reset by each call), else within one ulp (the dQ tiles are
-    added in arrival order)."""
+    scratch array and must be reset by each call).  Otherwise the dQ tiles are added into the
+    fp32 accumulator in arrival order, so the two runs are compared on their fp32 results
+    (ATTN_FLAG_OUT_F32): dK and dV bitwise, dQ within 1e-5, where fp32 reordering noise of
+    values of order one lies (about 1e-6) and a scratch-layout error would not."""
     B, Hq, Hkv, N, d = 2, 8, 2, 1000, 128
     code = {"bf16": _lib.ATTN_BF16, "f16": _lib.ATTN_F16}[dtype]
-    flags = _lib.ATTN_FLAG_DETERMINISTIC if deterministic else 0
+    flags = _lib.ATTN_FLAG_DETERMINISTIC if deterministic else _lib.ATTN_FLAG_OUT_F32
+    odt = W.DTYPES[dtype] if deterministic else torch.float32
     stream = torch.cuda.current_stream().cuda_stream
     q, k, v, dout = (t.to(dev) for t in W.dense_inputs(B, Hq, Hkv, N, d, dtype, seed=5))
     o, lse = _fwd(q, k, v, causal, code, stream)
     # the existing entry point, workspace allocated by the caller
     nbytes = _lib.attn_bwd_workspace_bytes(B, Hq, N, d)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    ref = _grads(q, k, v)
+    ref = _grads(q, k, v, odt)
     st = _lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                        *(g.data_ptr() for g in ref), ws.data_ptr(), nbytes, B, Hq, Hkv, N, d, causal, 0.0, code,
                        flags, stream)
     assert st == _lib.ATTN_OK
     # the allocation-free entry point, twice in a row
     for call in range(2):
-        out = _grads(q, k, v)
+        out = _grads(q, k, v, odt)
         st = _lib.attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
                                    lse.data_ptr(), *(g.data_ptr() for g in out), B, Hq, Hkv, N, d, causal, 0.0, code,
                                    flags, stream)
@@ -78,7 +70,8 @@ def test_noalloc_backward_matches_workspace_backward_twice(dev, dtype, causal, d
         for name, a, r in zip(("dQ", "dK", "dV"), out, ref):
             assert bool(torch.isfinite(a).all()), (call, name)
             if name == "dQ" and not deterministic:
-                assert _within_one_ulp(a, r, W.DTYPES[dtype]), f"call {call} dQ: more than one ulp from attn_bwd"
+                err = float((a.double() - r.double()).abs().max())
+                assert err <= 1e-5, f"call {call} dQ: {err:.3e} from attn_bwd"
             else:
                 assert torch.equal(a, r), f"call {call} {name}: not bitwise equal to attn_bwd"
 
