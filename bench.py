@@ -431,7 +431,7 @@ def fp32_alu_peak(sm_count: int, sm_mhz: float) -> float:
 # Configurations timed after the main workload, each on its own (a few steps, inputs resident):
 # the forward-only configurations, the varlen forward, the long-context step and the fp32
 # CUDA-core forward at a size that is not launch-bound.
-EXTRA_WORKLOADS = ("mha_f16", "mha_f16_causal", "varlen_bf16", "long_bf16", "f32_bh256")
+EXTRA_WORKLOADS = ("mha_f16", "mha_f16_causal", "varlen_bf16", "long_bf16", "short_bf16", "f32_bh256")
 
 
 def time_extra(name, dev, lib, stream, sp, peaks, sm_count, sm_mhz, budget_s=0.4):
@@ -461,6 +461,24 @@ def time_extra(name, dev, lib, stream, sp, peaks, sm_count, sm_mhz, budget_s=0.4
         return ent
     tf = S.fwd_f / (per_call[0] * 1e-3) / 1e12
     ent.update({"fwd_ms": per_call[0], "fwd_tflops": tf, "fwd_frac_burst": tf / burst})
+    if wl.N <= 64 and not wl.varlen and "Nq" not in wl.extra:
+        # the short-sequence kernel is HBM-bound: Q, K, V read and O, LSE written once
+        es = 2
+        nbytes = wl.B * (2 * wl.Hq + 2 * wl.Hkv) * wl.N * wl.d * es + wl.B * wl.Hq * wl.N * 4
+        gbs = nbytes / (per_call[0] * 1e-3) / 1e9
+        ent["roofline"] = {"kernel": "fwd_short_kernel", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": nbytes,
+                           "peak_source": f"{peaks['source']} HBM copy"}
+        # the same shape on the general persistent kernel (ATTN_SHORT_KERNEL=0), for comparison
+        os.environ["ATTN_SHORT_KERNEL"] = "0"
+        try:
+            for _ in range(3):
+                run_step(S, stream)
+            _, per_gen, _ = time_steps(S, stream, K)
+        finally:
+            del os.environ["ATTN_SHORT_KERNEL"]
+        ent.update({"general_kernel_fwd_ms": per_gen[0],
+                    "general_kernel_fwd_tflops": S.fwd_f / (per_gen[0] * 1e-3) / 1e12})
     if "bwd_main" in names:
         i = names.index("bwd_main")
         bwd_ms = sum(per_call[1:])

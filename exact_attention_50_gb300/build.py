@@ -17,7 +17,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libattn_gb300.so")
 
 SOURCES = ["attn_api.cu", "fwd_tc_bf16.cu", "fwd_tc_f16.cu", "bwd_tc_bf16.cu", "bwd_tc_f16.cu", "kv_combine.cu",
-           "simt_f32.cu", "bwd_aux.cu", "attn_noalloc.cu"]
+           "simt_f32.cu", "bwd_aux.cu", "attn_noalloc.cu", "fwd_short.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

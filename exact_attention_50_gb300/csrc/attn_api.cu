@@ -137,6 +137,60 @@ float resolve_scale(float scale, int d) { return scale == 0.f ? 1.f / std::sqrt(
 
 attn_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+// The short-sequence kernel serves dense fp16 / bf16 forwards with N <= 64 unless the environment
+// sets ATTN_SHORT_KERNEL=0 (a switch to time the general kernel on the same shapes).
+bool short_kernel_enabled() {
+  const char* e = std::getenv("ATTN_SHORT_KERNEL");
+  return !(e && e[0] == '0' && e[1] == '\0');
+}
+
+// Dense forward of short sequences on the packing kernel: one unit is a (batch, kv head) with its
+// R = G * N query rows (adjacent in [B, Hq, N, d]) and its N keys.
+attn_status_t fwd_short(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int N, int d, int causal, float scale, attn_dtype_t dtype, unsigned flags, cudaStream_t s) {
+  const long long U = static_cast<long long>(B) * Hkv;
+  const int G = Hq / Hkv;
+  const long long R = static_cast<long long>(G) * N;
+  if (U * R > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  attn::ShortParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.status = status_word();
+  p.wait_ns = wait_limit_ns();
+  if (!p.status) return ATTN_ERR_CUDA;
+  p.U = static_cast<int>(U); p.N = N; p.R = static_cast<int>(R); p.G = G; p.d = d;
+  p.packed = R <= attn::kBM ? 1 : 0;
+  p.P = p.packed ? attn::kBM / p.R : 1;
+  p.row_tiles = p.packed ? 1 : (p.R + attn::kBM - 1) / attn::kBM;
+  p.n_items = p.packed ? (p.U + p.P - 1) / p.P : p.U * p.row_tiles;
+  p.box_q = p.packed ? p.P * p.R : attn::kBM;
+  p.box_k = p.packed ? p.P * N : N;
+  p.scale_log2 = resolve_scale(scale, d) * kLog2e;
+  p.out_f32 = (flags & ATTN_FLAG_OUT_F32) ? 1 : 0;
+  FwdMaps maps;
+  const uint64_t es = 2;
+  if (p.packed) {
+    const uint64_t dq[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(U * R)};
+    const uint64_t dk[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(U * N)};
+    const uint64_t st[1] = {static_cast<uint64_t>(d) * es};
+    const uint32_t bq[2] = {64, static_cast<uint32_t>(p.box_q)}, bk[2] = {64, static_cast<uint32_t>(p.box_k)};
+    if (!make_map(&maps.q, q, dtype, 2, dq, st, bq) || !make_map(&maps.k, k, dtype, 2, dk, st, bk) ||
+        !make_map(&maps.v, v, dtype, 2, dk, st, bk) || (!p.out_f32 && !make_map(&maps.o, o, dtype, 2, dq, st, bq)))
+      return ATTN_ERR_CUDA;
+  } else {
+    const uint64_t dq[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(R), static_cast<uint64_t>(U)};
+    const uint64_t dk[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(N), static_cast<uint64_t>(U)};
+    const uint64_t sq[2] = {static_cast<uint64_t>(d) * es, static_cast<uint64_t>(R) * d * es};
+    const uint64_t sk[2] = {static_cast<uint64_t>(d) * es, static_cast<uint64_t>(N) * d * es};
+    const uint32_t bq[3] = {64, attn::kBM, 1}, bk[3] = {64, static_cast<uint32_t>(N), 1};
+    if (!make_map(&maps.q, q, dtype, 3, dq, sq, bq) || !make_map(&maps.k, k, dtype, 3, dk, sk, bk) ||
+        !make_map(&maps.v, v, dtype, 3, dk, sk, bk) || (!p.out_f32 && !make_map(&maps.o, o, dtype, 3, dq, sq, bq)))
+      return ATTN_ERR_CUDA;
+  }
+  if (p.out_f32) maps.o = maps.q;  // unused: fp32 rows are stored by the threads
+  return from_cuda(attn::launch_fwd_short(maps, p, dtype, causal != 0, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -170,6 +224,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.out_f32 = (flags & ATTN_FLAG_OUT_F32) ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (f32) return from_cuda(attn::launch_fwd_f32(q, k, v, p, causal != 0, attn::kModeDense, s));
+  if (N <= 64 && short_kernel_enabled())
+    return fwd_short(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, dtype, flags, s);
   FwdMaps maps;
   if (!make_dense_map(&maps.q, q, dtype, B * Hq, N, d) || !make_dense_map(&maps.k, k, dtype, B * Hkv, N, d) ||
       !make_dense_map(&maps.v, v, dtype, B * Hkv, N, d))

@@ -88,8 +88,10 @@ struct FwdLayout {
   static constexpr int kOffX = kOffV + kStagesV * kTileBytes;  // exchange [2 slots][2 groups][128 rows]
   static constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
   // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
-  // s_free[2], p_full[2], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain, o_staged
-  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1 + 1;
+  // s_free[2], p_full[2], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain,
+  // o_staged[2] (per Q slot, so it cannot run two phases ahead of the store warp: a slot takes
+  // a new Q only after the store warp has written out the tile staged in it)
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1 + 2;
   // tmem base (u32), abort flag (int), wait limit (u64, ns)
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kBytes = kOffMisc + 16;
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* o_free = pv_done + 2;
   uint64_t* xch = o_free + 1;       // [quadrant][slot]: row-max / row-sum exchange, warps q and q + 4
   uint64_t* drain = xch + 8;
-  uint64_t* o_staged = drain + 1;  // the softmax warps have written a tile-stored item's O tile
+  uint64_t* o_staged = drain + 1;  // [Q slot]: the softmax warps have staged a tile-stored item's O
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
@@ -292,6 +294,7 @@ __global__ void __launch_bounds__(352, 1)
     for (int i = 0; i < 8; ++i) mbar_init(xch + i, 2);  // the two warps of a row quadrant
     mbar_init(drain, 1);
     mbar_init(o_staged, 8);
+    mbar_init(o_staged + 1, 8);
     abort_set(abort_flag, 0);
     wait_limit_set(abort_flag, p.wait_ns);
     mbar_init_fence();
@@ -505,13 +508,13 @@ __global__ void __launch_bounds__(352, 1)
     // ================================================================ output tile stores
     if (lane == 0 && tile_out) {
       tma_prefetch_desc(&tmO);
-      uint32_t ic = 0, nt = 0;  // items; items stored by tiles (o_staged phases)
+      uint32_t ic = 0, nt[2] = {0, 0};  // items; per Q slot, items stored by tiles (o_staged phases)
       for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
         const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
         if (!it.valid) continue;
         const uint32_t qs = ic++ % SQ;
         if (!tile_item(it)) continue;
-        if (!mbar_wait(o_staged, nt++ & 1, abort_flag, p.status)) break;
+        if (!mbar_wait(o_staged + qs, nt[qs]++ & 1, abort_flag, p.status)) break;
         for (int c = 0; c < kChunks; ++c) {
           const uint8_t* src = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
           if constexpr (VARLEN)  // map {d, T, H} over the [T, H, d] output
@@ -728,7 +731,7 @@ __global__ void __launch_bounds__(352, 1)
           }
         }
         fence_async_smem();
-        mbar_arrive_warp(o_staged);
+        mbar_arrive_warp(o_staged + ic % SQ);
       }
 #pragma unroll
       for (int c = 0; c < (tile ? 0 : DP / 64); ++c) {

@@ -67,6 +67,25 @@ cudaError_t launch_fwd_f32(const void* q, const void* k, const void* v, const Fw
 // LSE = -inf.
 cudaError_t launch_kv_combine(const FwdParams& p, attn_dtype_t dtype, bool causal, cudaStream_t stream);
 
+// Short sequences (N <= 64): units of one (batch, kv head) -- R = G * N query rows against N
+// keys -- packed P to a 128-row tile when R <= 128 (flat 2-D maps {d, U*R} and {d, U*N} with
+// boxes of exactly P*R and P*N rows), else one unit's 128-row block per item (3-D maps
+// {d, R, U} and {d, N, U}).
+struct ShortParams {
+  void* o;                 // [B,Hq,N,d] = flat [U*R, d]
+  float* lse;              // [B,Hq,N] = flat [U*R]; nullable
+  unsigned* status;
+  unsigned long long wait_ns;
+  int U, N, R, G, d;
+  int packed, P, row_tiles, n_items;
+  int box_q, box_k;        // rows of the query / output box and of the key / value box
+  float scale_log2;
+  int out_f32;
+};
+
+cudaError_t launch_fwd_short(const FwdMaps& maps, const ShortParams& p, attn_dtype_t dtype, bool causal,
+                             cudaStream_t stream);
+
 // Backward.
 struct BwdParams {
   const void* q;

@@ -63,6 +63,11 @@ WORKLOADS = {
                                   backward=True),
     "long_bf16": Workload("long_bf16 B1 Hq32 Hkv8 N32768 d128 bf16 causal fwd+bwd", "bf16", B=1,
                           Hq=32, Hkv=8, N=32768, d=128, causal=True, scale=None, backward=True),
+    # many short sequences (the short-sequence kernel): 6144 problems of 64 tokens, head_dim 64,
+    # the diffusion-model shape of the attention-operator article's section 2.3 (64 queries,
+    # 768 = 12 x 64 channels) as self-attention
+    "short_bf16": Workload("short_bf16 B512 H12 N64 d64 bf16 fwd", "bf16", B=512, Hq=12, Hkv=12, N=64, d=64,
+                           causal=False, scale=None),
     # decode against a KV cache: one new token per sequence, caches of U[16384, 32768] keys
     "decode_bf16": Workload("decode_bf16 B8 Hq32 Hkv8 Nq1 cache U[16384,32768] of 32768 d128 bf16", "bf16", B=8,
                             Hq=32, Hkv=8, N=32768, d=128, causal=True, scale=None,
