@@ -204,6 +204,22 @@ def oracle_sample(wl, seconds: float, seed: int = 0):
     oracle.build()
     oracle.set_num_threads(os.cpu_count() or 1)
     cores = oracle.num_threads()
+    if wl.extra.get("cross"):  # whole kv groups of one batch: fwd (KV-cache form) + cross bwd
+        Nq, G = wl.extra["Nq"], wl.G
+        q, k, v, _ = W.kvcache_inputs(1, G, 1, Nq, wl.N, wl.d, wl.dtype, None, seed=seed)
+        dout = torch.randn(1, G, Nq, wl.d, generator=W.generator(1)).to(q.dtype)
+        qn, kn, vn, dn = (t.double().numpy() for t in (q, k, v, dout))
+        per_group = W.kvcache_fwd_flops([wl.N], G, Nq, wl.d, wl.causal) * 3.5
+        t0, groups = time.perf_counter(), 0
+        while True:
+            oracle.fwd_kvcache(qn, kn, vn, None, wl.causal, wl.scale)
+            oracle.bwd_cross(qn, kn, vn, dn, wl.causal, wl.scale)
+            groups += 1
+            if time.perf_counter() - t0 >= seconds or groups >= wl.B * wl.Hkv:
+                break
+        dt = time.perf_counter() - t0
+        return per_group * groups / dt / 1e12, cores, \
+            f"{groups} of {wl.B * wl.Hkv} kv groups ({G} query heads, {Nq} x {wl.N}), fwd+bwd, fp64"
     if "Nq" in wl.extra:
         v_, sample = kv_oracle_sample(wl, seconds, seed)
         return v_, cores, sample
@@ -281,6 +297,33 @@ def setup_step(wl, dev, lib, sp, bwd_flags) -> Step:
     S = Step()
     dt_code = {"f32": 0, "f16": 1, "bf16": 2}[wl.dtype]
     scale = 0.0 if wl.scale is None else float(wl.scale)
+    if wl.extra.get("cross"):
+        # cross-attention: Nq queries against N keys, forward (the KV-cache call without cache
+        # lengths) and backward
+        Nq = wl.extra["Nq"]
+        q_h, k_h, v_h, _ = W.kvcache_inputs(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, wl.dtype, None, seed=0)
+        do_h = torch.randn(wl.B, wl.Hq, Nq, wl.d, generator=W.generator(1)).to(q_h.dtype)
+        q, k, v, dout = q_h.to(dev), k_h.to(dev), v_h.to(dev), do_h.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(wl.B, wl.Hq, Nq, dtype=torch.float32, device=dev)
+        fbytes = lib.attn_fwd_kvcache_workspace_bytes(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, 0)
+        fws = torch.empty(fbytes, dtype=torch.uint8, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bbytes = lib.attn_bwd_cross_workspace_bytes(wl.B, wl.Hq, Nq, wl.N, wl.d, dt_code, bwd_flags)
+        bws = torch.empty(bbytes, dtype=torch.uint8, device=dev)
+        S.host_in, S.dev_in, S.dev_out = [q_h, k_h, v_h, do_h], [q, k, v, dout], [o, dq, dk, dv]
+        S.calls = [("fwd_cross", lambda: lib.attn_fwd_kvcache(
+                        q.data_ptr(), k.data_ptr(), v.data_ptr(), None, o.data_ptr(), lse.data_ptr(), fws.data_ptr(),
+                        fbytes, wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, int(wl.causal), scale, 0, dt_code, 0, sp)),
+                   ("bwd_cross", lambda: lib.attn_bwd_cross(
+                       q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), bws.data_ptr(), bbytes, wl.B, wl.Hq, wl.Hkv, Nq,
+                       wl.N, wl.d, int(wl.causal), scale, dt_code, bwd_flags, sp))]
+        S.kernels = 2 + 3
+        S.fwd_f = W.kvcache_fwd_flops([wl.N] * wl.B, wl.Hq, Nq, wl.d, wl.causal)
+        S.bwd_f = 2.5 * S.fwd_f
+        S.dom = ("bwd_tc_kernel", 1, S.bwd_f)
+        return S
     if "Nq" in wl.extra:
         Nq = wl.extra["Nq"]
         q_h, k_h, v_h, cl_h = W.kvcache_inputs(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, wl.dtype, wl.extra["lens"],
@@ -431,7 +474,7 @@ def fp32_alu_peak(sm_count: int, sm_mhz: float) -> float:
 # Configurations timed after the main workload, each on its own (a few steps, inputs resident):
 # the forward-only configurations, the varlen forward, the long-context step and the fp32
 # CUDA-core forward at a size that is not launch-bound.
-EXTRA_WORKLOADS = ("mha_f16", "mha_f16_causal", "varlen_bf16", "long_bf16", "short_bf16", "f32_bh256")
+EXTRA_WORKLOADS = ("mha_f16", "mha_f16_causal", "varlen_bf16", "long_bf16", "short_bf16", "cross_bf16", "f32_bh256")
 
 
 def time_extra(name, dev, lib, stream, sp, peaks, sm_count, sm_mhz, budget_s=0.4):
@@ -461,7 +504,7 @@ def time_extra(name, dev, lib, stream, sp, peaks, sm_count, sm_mhz, budget_s=0.4
         return ent
     tf = S.fwd_f / (per_call[0] * 1e-3) / 1e12
     ent.update({"fwd_ms": per_call[0], "fwd_tflops": tf, "fwd_frac_burst": tf / burst})
-    if wl.N <= 64 and not wl.varlen and "Nq" not in wl.extra:
+    if wl.N <= 64 and not wl.varlen and "Nq" not in wl.extra:  # the short-sequence kernel
         # the short-sequence kernel is HBM-bound: Q, K, V read and O, LSE written once
         es = 2
         nbytes = wl.B * (2 * wl.Hq + 2 * wl.Hkv) * wl.N * wl.d * es + wl.B * wl.Hq * wl.N * 4
@@ -479,14 +522,15 @@ def time_extra(name, dev, lib, stream, sp, peaks, sm_count, sm_mhz, budget_s=0.4
             del os.environ["ATTN_SHORT_KERNEL"]
         ent.update({"general_kernel_fwd_ms": per_gen[0],
                     "general_kernel_fwd_tflops": S.fwd_f / (per_gen[0] * 1e-3) / 1e12})
-    if "bwd_main" in names:
-        i = names.index("bwd_main")
+    if len(names) > 1:
         bwd_ms = sum(per_call[1:])
-        main_tf = S.bwd_f / (per_call[i] * 1e-3) / 1e12
         ent.update({"bwd_ms": bwd_ms, "bwd_tflops": S.bwd_f / (bwd_ms * 1e-3) / 1e12,
                     "bwd_frac_burst": S.bwd_f / (bwd_ms * 1e-3) / 1e12 / burst,
-                    "bwd_main_ms": per_call[i], "bwd_main_tflops": main_tf, "bwd_main_frac_burst": main_tf / burst,
                     "step_tflops": (S.fwd_f + S.bwd_f) / (ms / K * 1e-3) / 1e12})
+    if "bwd_main" in names:
+        i = names.index("bwd_main")
+        main_tf = S.bwd_f / (per_call[i] * 1e-3) / 1e12
+        ent.update({"bwd_main_ms": per_call[i], "bwd_main_tflops": main_tf, "bwd_main_frac_burst": main_tf / burst})
     if S.lengths is not None and wl.varlen:
         ent["total_tokens"] = sum(S.lengths)
     del S
@@ -640,7 +684,9 @@ def run_ours(args, rank, world, local):
             cfg["deterministic"] = True
         if wl.varlen:
             cfg["total_tokens"] = sum(lengths)
-        if "Nq" in wl.extra:
+        if wl.extra.get("cross"):
+            cfg.update({"queries": wl.extra["Nq"], "keys": wl.N, "step": "cross-attention fwd + bwd"})
+        elif "Nq" in wl.extra:
             cfg.update({"queries_per_sequence": wl.extra["Nq"], "cache_capacity": wl.N,
                         "cache_tokens": sum(lengths), "num_splits": nsplit, "step": "one decode forward (forward kernel + split combine)"})
         metric = "attention TFLOP/s (fwd+bwd)" if len(names) > 1 else "attention TFLOP/s (fwd)"
@@ -667,7 +713,23 @@ def run_reference(args, rank, world):
     cores = oracle.num_threads()
     # one step = the oracle's fwd (+bwd) of one query head over its kv head (a slice of the
     # workload), rows sampled when a whole head would take too long
-    if "Nq" in wl.extra:
+    if wl.extra.get("cross"):
+        Nq, G = wl.extra["Nq"], wl.G
+        q, k, v, _ = W.kvcache_inputs(1, G, 1, Nq, wl.N, wl.d, wl.dtype, None, seed=0)
+        import torch
+        dout = torch.randn(1, G, Nq, wl.d, generator=W.generator(1)).to(q.dtype)
+        qn, kn, vn, dn = (t.double().numpy() for t in (q, k, v, dout))
+        rows_per_step = 64
+        rng = np.random.default_rng(0)
+
+        def step():  # sampled query rows of one kv group, forward only
+            rows = np.stack([np.zeros(rows_per_step, int), rng.integers(0, G, rows_per_step),
+                             rng.integers(0, Nq, rows_per_step)], 1)
+            qs = qn[:, rows[:, 1], rows[:, 2]][:, None]  # [1, 1, rows, d] as one head of queries
+            oracle.fwd_kvcache(qs, kn, vn, None, False, wl.scale)
+            return 4.0 * wl.d * wl.N * rows_per_step
+        sample = f"{rows_per_step} sampled query rows against all {wl.N} keys per step (fwd only, unmasked), fp64"
+    elif "Nq" in wl.extra:
         Nq = wl.extra["Nq"]
         q, k, v, cl = W.kvcache_inputs(wl.B, wl.Hq, wl.Hkv, Nq, wl.N, wl.d, wl.dtype, wl.extra["lens"], seed=0)
         L = int(cl.min())  # the shortest cache of the batch: one batch per step

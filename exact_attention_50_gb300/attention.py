@@ -106,8 +106,9 @@ def bwd(q, k, v, o, lse, dout, causal: bool, scale=None, out_f32: bool = False, 
 
 def bwd_cross(q, k, v, o, lse, dout, causal: bool, scale=None, out_f32: bool = False, workspace=None,
               deterministic: bool = False):
-    """Cross-attention backward (Nq <= Nk, bottom-right causal alignment).  q, o, dout
-    [B,Hq,Nq,d]; k, v [B,Hkv,Nk,d]; lse [B,Hq,Nq] from fwd_kvcache without cache lengths.
+    """Cross-attention backward (any Nq, Nk; bottom-right causal alignment: query i sees key j
+    iff j <= i + Nk - Nq).  q, o, dout [B,Hq,Nq,d]; k, v [B,Hkv,Nk,d]; lse [B,Hq,Nq] from
+    fwd_kvcache without cache lengths.  Query rows that see no key get dq = 0.
     Returns (dq, dk, dv)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _require(t, n, q.dtype)
@@ -240,8 +241,8 @@ class _AttnFn(torch.autograd.Function):
 
 def flash_attention(q, k, v, causal: bool = True, scale=None, deterministic: bool = False):
     """Exact attention of [B,Hq,Nq,d] queries over [B,Hkv,Nk,d] keys/values (Hq % Hkv == 0).
-    Nq != Nk is cross-attention, with the causal mask aligned to the last Nq keys (its backward
-    needs Nq <= Nk).  deterministic makes the backward's dq bitwise reproducible (slower)."""
+    Nq != Nk is cross-attention, with the causal mask aligned to the last Nq keys.
+    deterministic makes the backward's dq bitwise reproducible (slower)."""
     return _AttnFn.apply(q, k, v, causal, scale, bool(deterministic))
 
 

@@ -313,7 +313,7 @@ attn_status_t bwd_setup(BwdParams* p, void* workspace, size_t workspace_bytes, i
   p->dq_turn = reinterpret_cast<int*>(reinterpret_cast<char*>(p->delta) + round256(rows * sizeof(float)));
   p->deterministic = (flags & ATTN_FLAG_DETERMINISTIC) ? 1 : 0;
   p->wait_ns = wait_limit_ns();
-  p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->N = N; p->d = d; p->G = Hq / Hkv;
+  p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->N = N; p->Nk = N; p->d = d; p->G = Hq / Hkv;
   p->n_ktiles = (N + attn::kBN - 1) / attn::kBN;
   const BwdParams::Rows dense{d, static_cast<long long>(N) * d};
   p->lay_q = p->lay_kv = p->lay_o = p->lay_dq = p->lay_dkv = dense;
@@ -398,19 +398,14 @@ size_t attn_bwd_varlen_workspace_bytes(int total_tokens, int H, int d) {
 }
 
 size_t attn_bwd_cross_workspace_bytes(int B, int Hq, int Nq, int Nk, int d, attn_dtype_t dtype, unsigned flags) {
-  if (B <= 0 || Hq <= 0 || Nq <= 0 || Nk < Nq || d <= 0) return 0;
-  const size_t bwd = attn_bwd_workspace_bytes(B, Hq, Nk, d);
-  if (Nq == Nk) return bwd;
-  const size_t es = dtype == ATTN_F32 ? 4 : 2;
-  const size_t eo = (dtype == ATTN_F32 || (flags & ATTN_FLAG_OUT_F32)) ? 4 : es;
-  const size_t rows = static_cast<size_t>(B) * Hq * Nk;
-  return bwd + 3 * round256(rows * d * es) + round256(rows * sizeof(float)) + round256(rows * d * eo);
+  (void)dtype;
+  (void)flags;
+  if (B <= 0 || Hq <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return 0;
+  return attn_bwd_workspace_bytes(B, Hq, Nq, d);
 }
 
-// Cross-attention backward on the square kernels: with bottom-right alignment query i sees the
-// keys that row Nk - Nq + i of an Nk-query problem sees, so q, o, dout and lse are placed at
-// the end of Nk-row buffers whose leading rows are zero (dO = 0 and D = 0 there, so they add
-// nothing to dK and dV), attn_bwd runs on those, and dq is copied back out.
+// Cross-attention backward: the backward kernels walk Nq query rows against Nk keys per head
+// directly, with the bottom-right causal alignment (query i sees key j iff j <= i + Nk - Nq).
 attn_status_t attn_bwd_cross(const void* q, const void* k, const void* v, const void* o, const void* dout,
                              const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                              int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
@@ -419,38 +414,45 @@ attn_status_t attn_bwd_cross(const void* q, const void* k, const void* v, const 
   if (st != ATTN_OK) return st;
   if (B < 0 || Nq < 0 || Nk < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (flags & ~(ATTN_FLAG_OUT_F32 | ATTN_FLAG_DETERMINISTIC)) return ATTN_ERR_INVALID_ARG;
-  if (Nq > Nk) return ATTN_ERR_UNSUPPORTED;
-  if (B == 0 || Nq == 0) return ATTN_OK;
-  if (!all_aligned16({q, k, v, o, dout, dq, dk, dv}) || !lse || !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
-  if (!workspace || !aligned(workspace, 256) ||
-      workspace_bytes < attn_bwd_cross_workspace_bytes(B, Hq, Nq, Nk, d, dtype, flags))
-    return ATTN_ERR_INVALID_ARG;
-  const size_t bwd_bytes = attn_bwd_workspace_bytes(B, Hq, Nk, d);
+  if (B == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;
   if (Nq == Nk)
-    return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, bwd_bytes, B, Hq, Hkv, Nk, d, causal, scale,
+    return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, Nk, d, causal, scale,
                     dtype, flags, stream);
-  const size_t es = dtype == ATTN_F32 ? 4 : 2;
-  const size_t eo = (dtype == ATTN_F32 || (flags & ATTN_FLAG_OUT_F32)) ? 4 : es;
-  const size_t heads = static_cast<size_t>(B) * Hq, rows = heads * Nk, pad = static_cast<size_t>(Nk - Nq);
-  char* qp = static_cast<char*>(workspace) + bwd_bytes;
-  char* op = qp + round256(rows * d * es);
-  char* dop = op + round256(rows * d * es);
-  char* lsep = dop + round256(rows * d * es);
-  char* dqp = lsep + round256(rows * sizeof(float));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto place = [&](char* dst, const void* src, size_t row_bytes) -> bool {
-    return cudaMemset2DAsync(dst, Nk * row_bytes, 0, pad * row_bytes, heads, s) == cudaSuccess &&
-           cudaMemcpy2DAsync(dst + pad * row_bytes, Nk * row_bytes, src, Nq * row_bytes, Nq * row_bytes, heads,
-                             cudaMemcpyDeviceToDevice, s) == cudaSuccess;
-  };
-  if (!place(qp, q, d * es) || !place(op, o, d * es) || !place(dop, dout, d * es) ||
-      !place(lsep, lse, sizeof(float)))
-    return ATTN_ERR_CUDA;
-  st = attn_bwd(qp, k, v, op, dop, reinterpret_cast<const float*>(lsep), dqp, dk, dv, workspace, bwd_bytes, B, Hq,
-                Hkv, Nk, d, causal, scale, dtype, flags, stream);
+  const size_t eo = (dtype == ATTN_F32 || (flags & ATTN_FLAG_OUT_F32)) ? 4 : 2;
+  if (Nq == 0) {  // no query: dk = dv = 0
+    if (!all_aligned16({dk, dv})) return ATTN_ERR_INVALID_ARG;
+    const size_t bytes = static_cast<size_t>(B) * Hkv * Nk * d * eo;
+    if (cudaMemsetAsync(dk, 0, bytes, s) != cudaSuccess || cudaMemsetAsync(dv, 0, bytes, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  if (Nk == 0) {  // no key: every query row sees nothing, dq = 0
+    if (!all_aligned16({dq})) return ATTN_ERR_INVALID_ARG;
+    return from_cuda(cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * Hq * Nq * d * eo, s));
+  }
+  if (!all_aligned16({q, k, v, o, dout, dq, dk, dv}) || !lse || !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+  if ((Nk + 31) / 32 > 65535) return ATTN_ERR_UNSUPPORTED;
+  BwdParams p{};
+  st = bwd_setup(&p, workspace, workspace_bytes, B, Hq, Hkv, Nq, d, scale, dtype, flags);
   if (st != ATTN_OK) return st;
-  return from_cuda(cudaMemcpy2DAsync(dq, Nq * d * eo, dqp + pad * d * eo, Nk * d * eo, Nq * d * eo, heads,
-                                     cudaMemcpyDeviceToDevice, s));
+  p.Nk = Nk;
+  p.n_ktiles = (Nk + attn::kBN - 1) / attn::kBN;
+  p.lay_kv = p.lay_dkv = BwdParams::Rows{d, static_cast<long long>(Nk) * d};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  if (!(p.status = status_word())) return ATTN_ERR_CUDA;
+  cudaError_t e = attn::launch_bwd_preprocess(p, dtype, dtype != ATTN_F32, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dtype == ATTN_F32) return from_cuda(attn::launch_bwd_f32(p, causal != 0, s));
+  BwdMaps maps;
+  if (!make_dense_map(&maps.q, q, dtype, B * Hq, Nq, d) || !make_dense_map(&maps.k, k, dtype, B * Hkv, Nk, d) ||
+      !make_dense_map(&maps.v, v, dtype, B * Hkv, Nk, d) || !make_dense_map(&maps.dout, dout, dtype, B * Hq, Nq, d) ||
+      !make_acc_map(&maps.dq_acc, p.dq_acc, static_cast<long long>(B) * Hq * Nq, d))
+    return ATTN_ERR_CUDA;
+  e = attn::launch_bwd_tc(maps, p, dtype, causal != 0, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  return from_cuda(attn::launch_bwd_postprocess(p, dtype, s));
 }
 
 attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout, const float* lse,

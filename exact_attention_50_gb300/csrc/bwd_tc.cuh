@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(512, 1)
   // Dense: x = batch * kv head.  Varlen: x = sequence * head; the sequence is the diagonal block
   // [seq_start, seq_start + seq_len) of a B = 1, N = total_tokens problem (G = 1).
   const int kt = blockIdx.y;
-  int hkv, hq0, seq_start = 0, seq_len = p.N;  // kv head (row block), its first query head, sequence
+  // kv head (row block), its first query head; the sequence's start, its query and key counts
+  int hkv, hq0, seq_start = 0, seq_len = p.N, kv_len = p.Nk;
   if (p.cu_seqlens) {
     const int s = blockIdx.x / p.Hkv, hh = blockIdx.x % p.Hkv;
     const int c0 = p.cu_seqlens[s], c1 = p.cu_seqlens[s + 1];
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     seq_start = c0;
     seq_len = c1 - c0;
+    kv_len = seq_len;
     hkv = hh;
     hq0 = hh * p.G;
   } else {
@@ -167,8 +169,12 @@ __global__ void __launch_bounds__(512, 1)
   }
   const int N = p.N;
   const int n_q = (seq_len + kBM - 1) / kBM;
-  if (kt >= n_q) return;  // a key tile past this sequence's end (varlen): the whole CTA
-  const int qt0 = CAUSAL ? kt : 0;
+  if (kt * kBN >= kv_len) return;  // a key tile past this sequence's end (varlen): the whole CTA
+  // causal: query i sees key j iff j <= i + off (off = 0 for self-attention; cross-attention
+  // aligns the queries with the last keys), so the first query tile that sees key tile kt is
+  // the one holding query kt * 128 - off; every key tile is seen by the last query
+  const int off = kv_len - seq_len;
+  const int qt0 = CAUSAL ? max(0, (kt * kBN - off) >= 0 ? (kt * kBN - off) / kBM : 0) : 0;
   const int per_head = n_q - qt0;
   const int n_it = p.G * per_head;
 
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld32(tl + col + c * 32, r);
           tmem_ld_wait();
           tmem_reg_fence(r);
-          if (key < seq_len && c * 32 < p.d) {
+          if (key < kv_len && c * 32 < p.d) {
             const int ncol = min(32, p.d - c * 32);
             if (p.out_f32) {
               float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + kofs + c * 32);
@@ -466,7 +472,7 @@ __global__ void __launch_bounds__(512, 1)
     const int t = quad * 32 + lane;           // TMEM lane: key row
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const int key = kt * kBN + t;
-    const bool key_ok = key < seq_len;
+    const bool key_ok = key < kv_len;
     const float sl2 = p.scale_log2;
     // The next tile's row terms are loaded one tile ahead and used only when they are written to
     // shared memory at the start of that tile, so no thread waits for the loads in between.
@@ -506,8 +512,9 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld_wait();
         tmem_reg_fence(r0);
         tmem_reg_fence(r1);
-        // queries q < key are masked under causal: only the diagonal tile has any
-        const int lim = CAUSAL ? key - qt * kBM - half * 64 : -1;  // columns c < lim are masked
+        // queries q < key - off are masked under causal (only the tiles on the diagonal have any);
+        // a query row that sees no key at all (LSE = -inf) has every column masked here
+        const int lim = CAUSAL ? key - off - qt * kBM - half * 64 : -1;  // columns c < lim are masked
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const uint32_t raw = i < 32 ? r0[i] : r1[i - 32];

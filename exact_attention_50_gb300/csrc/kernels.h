@@ -105,6 +105,10 @@ struct BwdParams {
   unsigned* status;
   unsigned long long wait_ns;  // limit of any single pipeline wait (0: the 4 s default)
   int B, Hq, Hkv, N, d, G;
+  // Keys per head (dense): N for self-attention, else the cross-attention key count, with the
+  // bottom-right causal alignment: query i sees key j iff j <= i + (Nk - N).  Varlen: the
+  // sequences are self-attention (Nk == N == total_tokens).
+  int Nk;
   int n_ktiles;
   float scale, scale_log2;
   int out_f32;

@@ -265,11 +265,11 @@ __global__ void __launch_bounds__(128) fwd_f32_kv_kernel(const float* __restrict
 // Which (kv head, sequence) block x of the backward grid covers: dense x = batch * kv head
 // (the whole sequence), varlen x = sequence * head (a diagonal block of a B = 1 problem).
 struct BwdBlock {
-  int hq0, hkv, seq_start, L;
+  int hq0, hkv, seq_start, L, Lk;  // first query head, kv head, sequence start, query and key counts
   bool ok;
 };
 __device__ __forceinline__ BwdBlock bwd_block(const BwdParams& p, int x) {
-  BwdBlock r{0, 0, 0, p.N, true};
+  BwdBlock r{0, 0, 0, p.N, p.Nk, true};
   if (p.cu_seqlens) {
     const int s = x / p.Hkv, hh = x % p.Hkv;
     const int c0 = p.cu_seqlens[s], c1 = p.cu_seqlens[s + 1];
@@ -281,6 +281,7 @@ __device__ __forceinline__ BwdBlock bwd_block(const BwdParams& p, int x) {
     }
     r.seq_start = c0;
     r.L = c1 - c0;
+    r.Lk = r.L;
     r.hkv = hh;
     r.hq0 = hh * p.G;
   } else {
@@ -308,7 +309,9 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const BwdParams p) {
   // blockIdx.x = (kv block) * G + query head within the group
   const BwdBlock bb = bwd_block(p, blockIdx.x / p.G);
   if (!bb.ok) return;
-  const int hq = bb.hq0 + blockIdx.x % p.G, d = p.d, N = bb.L, s0 = bb.seq_start;
+  // query i sees key j iff j <= i + off under the causal mask (off = Nk - N: the queries are
+  // aligned with the last keys; 0 for self-attention)
+  const int hq = bb.hq0 + blockIdx.x % p.G, d = p.d, N = bb.L, Nk = bb.Lk, off = Nk - N, s0 = bb.seq_start;
   const int row0 = blockIdx.y * kRows;
   if (row0 >= N) return;  // past this sequence's end (varlen)
   const size_t qbase = static_cast<size_t>(hq) * p.N + s0;  // row statistics of this head
@@ -331,12 +334,12 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const BwdParams p) {
 #pragma unroll
     for (int i = 0; i < kColsPerLane; ++i) acc[r][i] = 0.f;
   }
-  const int n_keys = CAUSAL ? min(N, row0 + kRows) : N;
+  const int n_keys = CAUSAL ? max(0, min(Nk, row0 + kRows + off)) : Nk;
   for (int key0 = 0; key0 < n_keys; key0 += kTile) {
     __syncthreads();
     for (int idx = threadIdx.x; idx < kTile * d; idx += blockDim.x) {
       const int r = idx / d, c = idx % d;
-      const bool in = key0 + r < N;
+      const bool in = key0 + r < Nk;
       sK[r * dp1 + c] = in ? kh[(key0 + r) * p.lay_kv.row + c] : 0.f;
       sV[r * dp1 + c] = in ? vh[(key0 + r) * p.lay_kv.row + c] : 0.f;
     }
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const BwdParams p) {
         s = fmaf(sQ[lr * d + c], sK[lane * dp1 + c], s);
         dp = fmaf(sdO[lr * d + c], sV[lane * dp1 + c], dp);
       }
-      const bool masked = qrow >= N || key >= N || (CAUSAL && key > qrow);
+      const bool masked = qrow >= N || key >= Nk || (CAUSAL && key > qrow + off);
       const float pr = masked ? 0.f : exp2f(s * p.scale_log2 - lse2[r]);
       const float ds = pr * (dp - Dr[r]);
       for (int jj = 0; jj < kTile; ++jj) {
@@ -394,14 +397,14 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const BwdParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BwdBlock bb = bwd_block(p, blockIdx.x);
   if (!bb.ok) return;
-  const int d = p.d, N = bb.L, s0 = bb.seq_start;
+  const int d = p.d, N = bb.L, Nk = bb.Lk, off = Nk - N, s0 = bb.seq_start;
   const int key0 = blockIdx.y * kRows;
-  if (key0 >= N) return;  // past this sequence's end (varlen)
+  if (key0 >= Nk) return;  // past this sequence's end (varlen)
   const float* kh = k + bb.hkv * p.lay_kv.head + s0 * p.lay_kv.row;
   const float* vh = v + bb.hkv * p.lay_kv.head + s0 * p.lay_kv.row;
   for (int idx = threadIdx.x; idx < kRows * d; idx += blockDim.x) {
     const int r = idx / d, c = idx % d;
-    const bool in = key0 + r < N;
+    const bool in = key0 + r < Nk;
     sK[r * d + c] = in ? kh[(key0 + r) * p.lay_kv.row + c] : 0.f;
     sV[r * d + c] = in ? vh[(key0 + r) * p.lay_kv.row + c] : 0.f;
   }
@@ -415,7 +418,8 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const BwdParams p) {
     const size_t qbase = static_cast<size_t>(hq) * p.N + s0;  // row statistics of this head
     const float* qh = q + hq * p.lay_q.head + s0 * p.lay_q.row;
     const float* doh = dout + hq * p.lay_o.head + s0 * p.lay_o.row;
-    for (int qrow0 = CAUSAL ? (key0 / kTile) * kTile : 0; qrow0 < N; qrow0 += kTile) {
+    // causal: the first query that sees key key0 is key0 - off
+    for (int qrow0 = CAUSAL ? (max(0, key0 - off) / kTile) * kTile : 0; qrow0 < N; qrow0 += kTile) {
       __syncthreads();
       for (int idx = threadIdx.x; idx < kTile * d; idx += blockDim.x) {
         const int r = idx / d, c = idx % d;
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const BwdParams p) {
           s = fmaf(sQ[lane * dp1 + c], sK[lr * d + c], s);
           dp = fmaf(sdO[lane * dp1 + c], sV[lr * d + c], dp);
         }
-        const bool masked = qrow >= N || key >= N || (CAUSAL && key > qrow);
+        const bool masked = qrow >= N || key >= Nk || (CAUSAL && key > qrow + off);
         const float pr = masked ? 0.f : exp2f(s * p.scale_log2 - sLse[lane]);
         const float ds = pr * (dp - sD[lane]);
         for (int ii = 0; ii < kTile; ++ii) {
@@ -461,7 +465,7 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const BwdParams p) {
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const int key = key0 + warp * 8 + r;
-    if (key >= N) continue;
+    if (key >= Nk) continue;
 #pragma unroll
     for (int i = 0; i < kColsPerLane; ++i) {
       const int c = lane + 32 * i;
@@ -507,9 +511,10 @@ cudaError_t launch_fwd_f32(const void* q, const void* k, const void* v, const Fw
 cudaError_t launch_bwd_f32(const BwdParams& p, bool causal, cudaStream_t stream) {
   // dense: x = batch * heads; varlen: x = sequence * heads, y over the longest sequence
   const int xs = p.cu_seqlens ? p.nseq : p.B;
-  const int ny = ((p.cu_seqlens ? p.max_seqlen : p.N) + kRows - 1) / kRows;
-  const dim3 gq(xs * p.Hq, ny);
-  const dim3 gk(xs * p.Hkv, ny);
+  const int nyq = ((p.cu_seqlens ? p.max_seqlen : p.N) + kRows - 1) / kRows;
+  const int nyk = ((p.cu_seqlens ? p.max_seqlen : p.Nk) + kRows - 1) / kRows;
+  const dim3 gq(xs * p.Hq, nyq);
+  const dim3 gk(xs * p.Hkv, nyk);
   const size_t smem_q = sizeof(float) * (2 * kTile * (p.d + 1) + 2 * kRows * p.d);
   const size_t smem_k = sizeof(float) * (2 * kTile * (p.d + 1) + 2 * kRows * p.d + 2 * kTile);
   auto kq = causal ? bwd_dq_f32_kernel<true> : bwd_dq_f32_kernel<false>;

@@ -68,6 +68,11 @@ WORKLOADS = {
     # 768 = 12 x 64 channels) as self-attention
     "short_bf16": Workload("short_bf16 B512 H12 N64 d64 bf16 fwd", "bf16", B=512, Hq=12, Hkv=12, N=64, d=64,
                            causal=False, scale=None),
+    # prefill against a cache (cross-attention forward and backward, Nq != Nk): a 2048-token chunk
+    # whose queries are the last 2048 positions of a 16384-key sequence (bottom-right causal mask)
+    "cross_bf16": Workload("cross_bf16 B2 Hq32 Hkv8 Nq2048 Nk16384 d128 bf16 causal fwd+bwd", "bf16", B=2, Hq=32,
+                           Hkv=8, N=16384, d=128, causal=True, scale=None, backward=True,
+                           extra={"Nq": 2048, "cross": True}),
     # decode against a KV cache: one new token per sequence, caches of U[16384, 32768] keys
     "decode_bf16": Workload("decode_bf16 B8 Hq32 Hkv8 Nq1 cache U[16384,32768] of 32768 d128 bf16", "bf16", B=8,
                             Hq=32, Hkv=8, N=32768, d=128, causal=True, scale=None,

@@ -179,16 +179,17 @@ attn_status_t attn_bwd_varlen(const void* qkv, const void* out, const void* dout
                               attn_dtype_t dtype, unsigned flags, void* stream);
 
 /*
- * Backward of cross-attention (the KV-cache forward above without cache lengths, Nq <= Nk),
- * with the same bottom-right causal alignment: gradients of q [B,Hq,Nq,d] and of k, v
- * [B,Hkv,Nk,d] for the forward's output o and LSE (natural log, [B,Hq,Nq]) and dL/do.
- * Under that alignment query i sees exactly the keys that row Nk - Nq + i of an Nk-query
- * problem sees, so the call runs attn_bwd on copies of q, o, dout and lse placed at the end of
- * Nk-row buffers with zero leading rows (which add nothing), then copies dq out.
+ * Backward of cross-attention (the KV-cache forward above without cache lengths): gradients of
+ * q [B,Hq,Nq,d] and of k, v [B,Hkv,Nk,d] for the forward's output o and LSE (natural log,
+ * [B,Hq,Nq]) and dL/do, for any Nq and Nk, with the same bottom-right causal alignment: query i
+ * sees key j iff j <= i + Nk - Nq.  The FlashAttention-T review names blocked KV-cache
+ * computation (FAQ 4) and the prefill phase (practical advice 2); the gradients are the
+ * backward's formulas restricted to the keys each query sees.  The backward kernels walk the
+ * Nq x Nk problem directly (no padded copies); a query row that sees no key (Nq > Nk under the
+ * causal mask, or Nk == 0) gets dq = 0, and with Nq == 0, dk = dv = 0.
  *   workspace  DEVICE, at least attn_bwd_cross_workspace_bytes(B, Hq, Nq, Nk, d, dtype, flags)
- *              bytes, 256-byte aligned
- * Nq > Nk returns ATTN_ERR_UNSUPPORTED; Nq == Nk is attn_bwd.  Flags, layouts and the other
- * argument rules are those of attn_bwd.
+ *              bytes (that of attn_bwd for Nq query rows), 256-byte aligned
+ * Nq == Nk is attn_bwd.  Flags, layouts and the other argument rules are those of attn_bwd.
  */
 size_t attn_bwd_cross_workspace_bytes(int B, int Hq, int Nq, int Nk, int d, attn_dtype_t dtype, unsigned flags);
 attn_status_t attn_bwd_cross(const void* q, const void* k, const void* v, const void* o, const void* dout,

@@ -199,14 +199,11 @@ def test_kvcache_splits_workspace_and_validation(lib):
 
 def test_bwd_cross_workspace_and_validation(lib):
     W = _lib.attn_bwd_cross_workspace_bytes
-    r256 = lambda x: (x + 255) // 256 * 256
-    assert W(2, 4, 100, 100, 64, _lib.ATTN_BF16, 0) == _lib.attn_bwd_workspace_bytes(2, 4, 100, 64)
-    rows = 2 * 4 * 300
-    assert W(2, 4, 100, 300, 64, _lib.ATTN_BF16, 0) == (_lib.attn_bwd_workspace_bytes(2, 4, 300, 64)
-                                                       + 3 * r256(rows * 64 * 2) + r256(rows * 4) + r256(rows * 64 * 2))
-    assert W(2, 4, 100, 300, 64, _lib.ATTN_BF16, _lib.ATTN_FLAG_OUT_F32) == (
-        _lib.attn_bwd_workspace_bytes(2, 4, 300, 64) + 3 * r256(rows * 64 * 2) + r256(rows * 4) + r256(rows * 64 * 4))
-    assert W(2, 4, 301, 300, 64, _lib.ATTN_BF16, 0) == 0  # Nq > Nk is not provided
+    # the kernels walk Nq x Nk directly: the workspace is attn_bwd's for the Nq query rows
+    for Nq, Nk in ((100, 100), (100, 300), (301, 300), (1, 5000)):
+        for flags in (0, _lib.ATTN_FLAG_OUT_F32):
+            assert W(2, 4, Nq, Nk, 64, _lib.ATTN_BF16, flags) == _lib.attn_bwd_workspace_bytes(2, 4, Nq, 64)
+    assert W(2, 4, 0, 300, 64, _lib.ATTN_BF16, 0) == 0
     ws = W(2, 4, 100, 300, 64, _lib.ATTN_BF16, 0)
 
     def f(**kw):
@@ -215,8 +212,8 @@ def test_bwd_cross_workspace_and_validation(lib):
         return _lib.attn_bwd_cross(a["p"], a["p"], a["p"], a["p"], a["p"], a["lse"], a["p"], a["p"], a["p"], a["ws"],
                                    a["wsb"], a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nk"], a["d"], 1, 0.0,
                                    _lib.ATTN_BF16, a["flags"], None)
-    assert f(Nq=301) == _lib.ATTN_ERR_UNSUPPORTED
-    assert f(B=0) == _lib.ATTN_OK and f(Nq=0) == _lib.ATTN_OK
+    assert f(B=0) == _lib.ATTN_OK and f(Nq=0, Nk=0) == _lib.ATTN_OK
+    assert f(Nq=301, wsb=W(2, 4, 301, 300, 64, _lib.ATTN_BF16, 0) - 1) == _lib.ATTN_ERR_INVALID_ARG
     assert f(p=4100) == _lib.ATTN_ERR_INVALID_ARG
     assert f(lse=None) == _lib.ATTN_ERR_INVALID_ARG
     assert f(wsb=ws - 1) == _lib.ATTN_ERR_INVALID_ARG
