@@ -39,15 +39,39 @@ __device__ __forceinline__ void warp_max_sum(float& v, bool is_max) {
 }
 
 // ------------------------------------------------------------------ forward
-template <bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(128) fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+// Register-tiled FFMA forward: a CTA of 256 threads owns 64 query rows and walks the keys in
+// tiles of 64.  Thread (ty, tx) = (t / 16, t % 16) owns rows 4 ty .. 4 ty + 3; for S = Q K^T it
+// computes the 4 x 4 block of keys 4 tx .. 4 tx + 3 (Q and K staged transposed, so each step
+// over the head dimension is one float4 of Q and one of K for 16 FMAs), and for O it owns the
+// columns 4 tx .. 4 tx + 3 (and 64 + 4 tx .. when d > 64).  A row's max and sum are reduced
+// over the 16 threads of its half-warp with shuffles; P goes through shared memory (over the
+// K^T area, free once S is computed) to the P V product.  Online softmax in base 2 with
+// log2(e) folded into the scale.  About 101 KB of shared memory at d = 128: two CTAs per SM.
+constexpr int kBM32 = 64, kBN32 = 64, kPad32 = 4;
+
+template <int DMAX>
+struct F32Layout {
+  static constexpr int kQt = 0;                                   // [DMAX][kBM32 + pad]: Q^T
+  static constexpr int kKt = kQt + DMAX * (kBM32 + kPad32);       // [DMAX][kBN32 + pad]: K^T
+  static constexpr int kP = kKt;  // [kBM32][kBN32 + pad]: P over K^T, once S is computed
+  static constexpr int kV = kKt + DMAX * (kBN32 + kPad32);        // [kBN32][DMAX + pad]
+  static constexpr int kFloats = kV + kBN32 * (DMAX + kPad32);
+  static_assert(DMAX * (kBN32 + kPad32) >= kBM32 * (kBN32 + kPad32), "P must fit in the K^T area");
+};
+
+template <bool CAUSAL, bool VARLEN, int DMAX>
+__global__ void __launch_bounds__(256) fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                                                       const float* __restrict__ v, const FwdParams p) {
-  extern __shared__ float smem_f[];
-  const int dp1 = p.d + 1;
-  float* sK = smem_f;                  // [kTile][d+1]
-  float* sV = sK + kTile * dp1;        // [kTile][d]
-  float* sQ = sV + kTile * p.d;        // [kRows][d]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  using L = F32Layout<DMAX>;
+  constexpr int SQ = kBM32 + kPad32, SK = kBN32 + kPad32, SV = DMAX + kPad32, SP = kBN32 + kPad32;
+  constexpr int NC = DMAX / 64;  // float4 column groups of O per thread
+  extern __shared__ float4 smem_f4[];
+  float* smem = reinterpret_cast<float*>(smem_f4);
+  float* sQt = smem + L::kQt;
+  float* sKt = smem + L::kKt;
+  float* sV = smem + L::kV;
+  float* sP = smem + L::kP;
+  const int t = threadIdx.x, tx = t & 15, ty = t >> 4;
   int b = 0, h, seq_start = 0, seq_len;
   const int qt = blockIdx.y;
   if constexpr (VARLEN) {
@@ -62,98 +86,160 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(const float* __restrict__ 
     }
     seq_start = c0;
     seq_len = c1 - c0;
-    if (qt * kRows >= seq_len) return;
+    if (qt * kBM32 >= seq_len) return;
   } else {
     b = blockIdx.x / p.Hq;
     h = blockIdx.x % p.Hq;
     seq_len = p.N;
   }
-  const int d = p.d, g = h / p.G;
-  RowAddr qa, ka, va;
+  const int d = p.d, g = h / p.G, d4 = d / 4;
+  RowAddr qa, ka;
   if constexpr (VARLEN) {
     // q, k and v already point at planes 0, 1 and 2 of the packed [T,3,H,d] tensor
     const size_t tok = 3ull * p.Hq * d;
     qa = {static_cast<size_t>(seq_start) * tok + static_cast<size_t>(h) * d, tok};
     ka = qa;
-    va = qa;
   } else {
     qa = {(static_cast<size_t>(b) * p.Hq + h) * p.N * d, static_cast<size_t>(d)};
     ka = {(static_cast<size_t>(b) * p.Hkv + g) * p.N * d, static_cast<size_t>(d)};
-    va = ka;
   }
-  const int row0 = qt * kRows;
-  for (int idx = threadIdx.x; idx < kRows * d; idx += blockDim.x) {
-    const int r = idx / d, c = idx % d;
-    sQ[r * d + c] = (row0 + r < seq_len) ? q[qa.base + (row0 + r) * qa.stride + c] : 0.f;
+  const int row0 = qt * kBM32;
+  // Q^T: column c of row r at sQt[c][r]; a warp stores 32 consecutive rows of one column group
+  for (int idx = t; idx < kBM32 * (DMAX / 4); idx += 256) {
+    const int r = idx % kBM32, c4 = idx / kBM32;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row0 + r < seq_len && c4 < d4) x = *reinterpret_cast<const float4*>(q + qa.base + (row0 + r) * qa.stride + 4 * c4);
+    sQt[(4 * c4 + 0) * SQ + r] = x.x;
+    sQt[(4 * c4 + 1) * SQ + r] = x.y;
+    sQt[(4 * c4 + 2) * SQ + r] = x.z;
+    sQt[(4 * c4 + 3) * SQ + r] = x.w;
   }
-  float m[8], l[8], acc[8][kColsPerLane];
+  float m[4], l[4], o[4][4 * NC];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.f;
+  for (int i = 0; i < 4; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
 #pragma unroll
-    for (int i = 0; i < kColsPerLane; ++i) acc[r][i] = 0.f;
+    for (int c = 0; c < 4 * NC; ++c) o[i][c] = 0.f;
   }
   const float sl2 = p.scale_log2;
-  const int row_hi = min(seq_len, row0 + kRows) - 1;
+  const int row_hi = min(seq_len, row0 + kBM32) - 1;
   const int n_keys = CAUSAL ? min(seq_len, row_hi + 1) : seq_len;
-  for (int key0 = 0; key0 < n_keys; key0 += kTile) {
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < kTile * d; idx += blockDim.x) {
-      const int r = idx / d, c = idx % d;
-      const bool in = key0 + r < seq_len;
-      sK[r * dp1 + c] = in ? k[ka.base + (key0 + r) * ka.stride + c] : 0.f;
-      sV[r * d + c] = in ? v[va.base + (key0 + r) * va.stride + c] : 0.f;
+  for (int key0 = 0; key0 < n_keys; key0 += kBN32) {
+    __syncthreads();  // the previous tile's K, V and P are no longer read
+    for (int idx = t; idx < kBN32 * (DMAX / 4); idx += 256) {
+      const int r = idx % kBN32, c4 = idx / kBN32;
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (key0 + r < seq_len && c4 < d4) x = *reinterpret_cast<const float4*>(k + ka.base + (key0 + r) * ka.stride + 4 * c4);
+      sKt[(4 * c4 + 0) * SK + r] = x.x;
+      sKt[(4 * c4 + 1) * SK + r] = x.y;
+      sKt[(4 * c4 + 2) * SK + r] = x.z;
+      sKt[(4 * c4 + 3) * SK + r] = x.w;
+    }
+    for (int idx = t; idx < kBN32 * (DMAX / 4); idx += 256) {
+      const int r = idx / (DMAX / 4), c4 = idx % (DMAX / 4);
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (key0 + r < seq_len && c4 < d4) x = *reinterpret_cast<const float4*>(v + ka.base + (key0 + r) * ka.stride + 4 * c4);
+      *reinterpret_cast<float4*>(sV + r * SV + 4 * c4) = x;
     }
     __syncthreads();
-    const int key = key0 + lane;
+    // ---- S block: rows 4 ty + i, keys 4 tx + j
+    float sblk[4][4];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int lr = warp * 8 + r, qrow = row0 + lr;
-      float s = 0.f;
-      for (int c = 0; c < d; ++c) s = fmaf(sQ[lr * d + c], sK[lane * dp1 + c], s);
-      const bool masked = key >= seq_len || (CAUSAL && key > qrow);
-      float x = masked ? -INFINITY : s * sl2;
-      float mx = x;
-      warp_max_sum(mx, true);
-      const float m_new = fmaxf(m[r], mx);
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sblk[i][j] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < d; ++c) {
+      const float4 qv = *reinterpret_cast<const float4*>(sQt + c * SQ + 4 * ty);
+      const float4 kv = *reinterpret_cast<const float4*>(sKt + c * SK + 4 * tx);
+      const float qq[4] = {qv.x, qv.y, qv.z, qv.w}, kk[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sblk[i][j] = fmaf(qq[i], kk[j], sblk[i][j]);
+    }
+    __syncthreads();  // every thread is done with K^T: P goes over it
+    // ---- online softmax over the tile (a row lives on the 16 threads of a half-warp)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int qrow = row0 + 4 * ty + i;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int key = key0 + 4 * tx + j;
+        const bool masked = key >= seq_len || (CAUSAL && key > qrow);
+        sblk[i][j] = masked ? -INFINITY : sblk[i][j] * sl2;
+        mx = fmaxf(mx, sblk[i][j]);
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_new = fmaxf(m[i], mx);
       const float mb = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = exp2f(m[r] - mb);
-      const float pr = exp2f(x - mb);
-      float rs = pr;
-      warp_max_sum(rs, false);
-      l[r] = l[r] * alpha + rs;
-      m[r] = m_new;
+      const float alpha = exp2f(m[i] - mb);
+      float rs = 0.f;
 #pragma unroll
-      for (int i = 0; i < kColsPerLane; ++i) acc[r][i] *= alpha;
-      for (int jj = 0; jj < kTile; ++jj) {
-        const float pj = __shfl_sync(0xffffffffu, pr, jj);
+      for (int j = 0; j < 4; ++j) {
+        sblk[i][j] = exp2f(sblk[i][j] - mb);
+        rs += sblk[i][j];
+      }
 #pragma unroll
-        for (int i = 0; i < kColsPerLane; ++i) {
-          const int c = lane + 32 * i;
-          if (c < d) acc[r][i] = fmaf(pj, sV[jj * d + c], acc[r][i]);
+      for (int off = 8; off > 0; off >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, off);
+      l[i] = l[i] * alpha + rs;
+      m[i] = m_new;
+#pragma unroll
+      for (int c = 0; c < 4 * NC; ++c) o[i][c] *= alpha;
+      *reinterpret_cast<float4*>(sP + (4 * ty + i) * SP + 4 * tx) =
+          make_float4(sblk[i][0], sblk[i][1], sblk[i][2], sblk[i][3]);
+    }
+    __syncthreads();
+    // ---- O += P V: rows 4 ty + i, columns 4 tx + j (+ 64 when d > 64)
+    const int kn = min(kBN32, seq_len - key0);
+    for (int kb = 0; kb < kn; kb += 4) {
+      float4 pr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pr[i] = *reinterpret_cast<const float4*>(sP + (4 * ty + i) * SP + kb);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        float vv[4 * NC];
+#pragma unroll
+        for (int cg = 0; cg < NC; ++cg) {
+          const float4 x = *reinterpret_cast<const float4*>(sV + (kb + kk) * SV + 64 * cg + 4 * tx);
+          vv[4 * cg + 0] = x.x;
+          vv[4 * cg + 1] = x.y;
+          vv[4 * cg + 2] = x.z;
+          vv[4 * cg + 3] = x.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float pk = kk == 0 ? pr[i].x : kk == 1 ? pr[i].y : kk == 2 ? pr[i].z : pr[i].w;
+#pragma unroll
+          for (int c = 0; c < 4 * NC; ++c) o[i][c] = fmaf(pk, vv[c], o[i][c]);
         }
       }
     }
   }
+  // ---- epilogue: O / l, LSE
+  float* out = static_cast<float*>(p.o);
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int qrow = row0 + warp * 8 + r;
+  for (int i = 0; i < 4; ++i) {
+    const int qrow = row0 + 4 * ty + i;
     if (qrow >= seq_len) continue;
-    const float inv_l = 1.f / l[r];
+    const float inv_l = 1.f / l[i];
     size_t out_off;
     if constexpr (VARLEN)
       out_off = (static_cast<size_t>(seq_start + qrow) * p.Hq + h) * d;
     else
       out_off = ((static_cast<size_t>(b) * p.Hq + h) * p.N + qrow) * d;
-    float* o = static_cast<float*>(p.o);
 #pragma unroll
-    for (int i = 0; i < kColsPerLane; ++i) {
-      const int c = lane + 32 * i;
-      if (c < d) o[out_off + c] = acc[r][i] * inv_l;
+    for (int cg = 0; cg < NC; ++cg) {
+      const int c = 64 * cg + 4 * tx;
+      if (c < d)
+        *reinterpret_cast<float4*>(out + out_off + c) =
+            make_float4(o[i][4 * cg] * inv_l, o[i][4 * cg + 1] * inv_l, o[i][4 * cg + 2] * inv_l, o[i][4 * cg + 3] * inv_l);
     }
-    if (lane == 0 && p.lse) {
-      const float lse = (m[r] + log2f(l[r])) / kLog2e;
+    if (tx == 0 && p.lse) {
+      const float lse = (m[i] + log2f(l[i])) / kLog2e;
       if constexpr (VARLEN)
         p.lse[static_cast<size_t>(h) * p.total_tokens + seq_start + qrow] = lse;
       else
@@ -500,12 +586,30 @@ cudaError_t launch_fwd_f32(const void* q, const void* k, const void* v, const Fw
     const dim3 grid(p.B * p.Hq, (p.Nq + kRows - 1) / kRows, p.n_splits);
     return causal ? run(fwd_f32_kv_kernel<true>, grid) : run(fwd_f32_kv_kernel<false>, grid);
   }
-  if (mode == kModeVarlen) {
-    const dim3 grid(p.Hq, (p.max_seqlen + kRows - 1) / kRows, p.nseq);
-    return causal ? run(fwd_f32_kernel<true, true>, grid) : run(fwd_f32_kernel<false, true>, grid);
+  // dense and varlen: the register-tiled kernel, 64 query rows per CTA
+  auto run_tiled = [&](auto kern, dim3 grid, size_t bytes) -> cudaError_t {
+    cudaError_t e = set_smem(kern, bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 256, bytes, stream>>>(qf, kf, vf, p);
+    return cudaGetLastError();
+  };
+  const bool varlen = mode == kModeVarlen;
+  const dim3 grid = varlen ? dim3(p.Hq, (p.max_seqlen + kBM32 - 1) / kBM32, p.nseq)
+                           : dim3(p.B * p.Hq, (p.N + kBM32 - 1) / kBM32, 1);
+  if (p.d <= 64) {
+    const size_t bytes = sizeof(float) * F32Layout<64>::kFloats;
+    if (varlen)
+      return causal ? run_tiled(fwd_f32_kernel<true, true, 64>, grid, bytes)
+                    : run_tiled(fwd_f32_kernel<false, true, 64>, grid, bytes);
+    return causal ? run_tiled(fwd_f32_kernel<true, false, 64>, grid, bytes)
+                  : run_tiled(fwd_f32_kernel<false, false, 64>, grid, bytes);
   }
-  const dim3 grid(p.B * p.Hq, (p.N + kRows - 1) / kRows, 1);
-  return causal ? run(fwd_f32_kernel<true, false>, grid) : run(fwd_f32_kernel<false, false>, grid);
+  const size_t bytes = sizeof(float) * F32Layout<128>::kFloats;
+  if (varlen)
+    return causal ? run_tiled(fwd_f32_kernel<true, true, 128>, grid, bytes)
+                  : run_tiled(fwd_f32_kernel<false, true, 128>, grid, bytes);
+  return causal ? run_tiled(fwd_f32_kernel<true, false, 128>, grid, bytes)
+                : run_tiled(fwd_f32_kernel<false, false, 128>, grid, bytes);
 }
 
 cudaError_t launch_bwd_f32(const BwdParams& p, bool causal, cudaStream_t stream) {
