@@ -495,9 +495,10 @@ __global__ void __launch_bounds__(512, 1)
       const int qt = qt0 + it % per_head;
       float* lse_buf = sLse + (it & 1) * 128;
       float* d_buf = sD + (it & 1) * 128;
+      // stored negated, so each element needs one paired FMA (and one paired add) against them
       if (threadIdx.x < 128) {
-        lse_buf[threadIdx.x] = row_next ? lse_next * 1.4426950408889634f : INFINITY;
-        d_buf[threadIdx.x] = row_next ? d_next : 0.f;
+        lse_buf[threadIdx.x] = row_next ? -(lse_next * 1.4426950408889634f) : -INFINITY;
+        d_buf[threadIdx.x] = row_next ? -d_next : 0.f;
       }
       mbar_arrive_warp(rows_ready);
       if (!mbar_wait_warp(rows_ready, it & 1, abort_flag, p.status)) break;
@@ -512,15 +513,33 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld_wait();
         tmem_reg_fence(r0);
         tmem_reg_fence(r1);
-        // queries q < key - off are masked under causal (only the tiles on the diagonal have any);
-        // a query row that sees no key at all (LSE = -inf) has every column masked here
-        const int lim = CAUSAL ? key - off - qt * kBM - half * 64 : -1;  // columns c < lim are masked
+        // P = 2^(S scale log2e - LSE log2e): the row terms as float4 from shared memory, the
+        // argument as one paired FMA per two queries
+        const float4* nl4 = reinterpret_cast<const float4*>(lse_buf + half * 64);
+        const uint64_t scl = f2_pack(sl2, sl2);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const uint32_t raw = i < 32 ? r0[i] : r1[i - 32];
-          float pr = ex2_approx(fmaf(__uint_as_float(raw), sl2, -lse_buf[half * 64 + i]));
-          if (i < lim) pr = 0.f;
-          pv[i] = key_ok ? pr : 0.f;
+        for (int i4 = 0; i4 < 16; ++i4) {
+          const float4 nl = nl4[i4];
+          const int i = 4 * i4;
+          const float s0 = __uint_as_float(i < 32 ? r0[i] : r1[i - 32]);
+          const float s1 = __uint_as_float(i < 32 ? r0[i + 1] : r1[i - 31]);
+          const float s2 = __uint_as_float(i < 32 ? r0[i + 2] : r1[i - 30]);
+          const float s3 = __uint_as_float(i < 32 ? r0[i + 3] : r1[i - 29]);
+          const float2 x01 = f2_unpack(f2_fma(f2_pack(s0, s1), scl, f2_pack(nl.x, nl.y)));
+          const float2 x23 = f2_unpack(f2_fma(f2_pack(s2, s3), scl, f2_pack(nl.z, nl.w)));
+          pv[i] = ex2_approx(x01.x);
+          pv[i + 1] = ex2_approx(x01.y);
+          pv[i + 2] = ex2_approx(x23.x);
+          pv[i + 3] = ex2_approx(x23.y);
+        }
+        // queries q < key - off are masked under causal (only tiles on the diagonal have any; a
+        // query row that sees no key at all has every column masked), and keys past the
+        // sequence give P = 0: the selects run only where a thread has such columns
+        // columns c < lim are masked (a key past the sequence: all 64)
+        const int lim = !key_ok ? 64 : (CAUSAL ? key - off - qt * kBM - half * 64 : -1);
+        if (lim > 0) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) pv[i] = i < lim ? 0.f : pv[i];
         }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -547,10 +566,16 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld_wait();
         tmem_reg_fence(r0);
         tmem_reg_fence(r1);
+        // dS = P (dP - D), with D (stored negated) read as float4
+        const float4* nd4 = reinterpret_cast<const float4*>(d_buf + half * 64);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const uint32_t raw = i < 32 ? r0[i] : r1[i - 32];
-          pv[i] = pv[i] * (__uint_as_float(raw) - d_buf[half * 64 + i]);
+        for (int i4 = 0; i4 < 16; ++i4) {
+          const float4 nd = nd4[i4];
+          const int i = 4 * i4;
+          pv[i] *= __uint_as_float(i < 32 ? r0[i] : r1[i - 32]) + nd.x;
+          pv[i + 1] *= __uint_as_float(i < 32 ? r0[i + 1] : r1[i - 31]) + nd.y;
+          pv[i + 2] *= __uint_as_float(i < 32 ? r0[i + 2] : r1[i - 30]) + nd.z;
+          pv[i + 3] *= __uint_as_float(i < 32 ? r0[i + 3] : r1[i - 29]) + nd.w;
         }
       }
       tc_fence_before();  // the dP columns are consumed (the dQ MMA may overwrite them)
