@@ -14,7 +14,7 @@
 // mask are applied inside the GEMM loop as in its best practice 2.
 //
 // A CTA loops over 128-row query tiles, numbered heaviest first under the causal mask and
-// dealt to the CTAs in snake order (cta_item).  352 threads:
+// dealt to the CTAs in snake order (cta_item).  384 threads:
 //   warps 0-3  softmax, key columns 0-63 of each S tile; warps 4-7 softmax, key columns 64-127.
 //              Thread t of either group owns query row t (TMEM lane t).  The two threads of a
 //              row exchange their partial row maxima through shared memory, so both use the
@@ -23,9 +23,10 @@
 //              rescales its half of the O row when the max moved, and at the end normalises
 //              that half of O: into the item's Q slot for a tile store, or to global memory.
 //   warp 8     TMA producer (lane 0) and TMEM allocator (whole warp).
-//   warp 9     MMA issuer (lane 0): a non-blocking scheduler over the streams S(j) and PV(j).
+//   warp 9     MMA issuer of the S(j) stream (lane 0).
 //   warp 10    output tile stores (lane 0): writes each staged O tile with TMA and frees the
 //              Q slot.
+//   warp 11    MMA issuer of the PV(j) stream (lane 0).
 // TMEM: S double buffer at columns [0,128) and [128,256), P double buffer (16-bit pairs) at
 // [256,320) and [320,384), O at [384, 384+DP).  S(j) goes into S buffer j % 2 as soon as the
 // softmax has loaded S(j-2) into registers, and P(j) into P buffer j % 2 once PV(j-2) has read
@@ -91,15 +92,15 @@ struct FwdLayout {
   // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
   // s_free[2], p_full[2], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain,
   // o_staged[2] (per Q slot, so it cannot run two phases ahead of the store warp: a slot takes
-  // a new Q only after the store warp has written out the tile staged in it)
-  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1 + 2;
+  // a new Q only after the store warp has written out the tile staged in it), drain2
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1 + 2 + 1;
   // tmem base (u32), abort flag (int), wait limit (u64, ns)
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColP = 256, kColO = 384;
-  static constexpr int kThreads = 352;
+  static constexpr int kThreads = 384;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -237,7 +238,7 @@ struct TileCursor {
 };
 
 template <typename T, int DP, bool CAUSAL, int MODE>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdParams p, int n_items) {
@@ -285,6 +286,7 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* xch = o_free + 1;       // [quadrant][slot]: row-max / row-sum exchange, warps q and q + 4
   uint64_t* drain = xch + 8;
   uint64_t* o_staged = drain + 1;  // [Q slot]: the softmax warps have staged a tile-stored item's O
+  uint64_t* drain2 = o_staged + 2;  // abort path of the PV issuer (drain: the S issuer)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
@@ -312,6 +314,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(o_free, 8);
     for (int i = 0; i < 8; ++i) mbar_init(xch + i, 2);  // the two warps of a row quadrant
     mbar_init(drain, 1);
+    mbar_init(drain2, 1);
     mbar_init(o_staged, 8);
     mbar_init(o_staged + 1, 8);
     abort_set(abort_flag, 0);
@@ -422,53 +425,21 @@ __global__ void __launch_bounds__(352, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
-    // ================================================================ MMA issuer
+  } else if (warp == 9 || warp == 11) {
+    // ================================================================ MMA issuers
+    // Two threads on two sub-partitions: warp 9 issues the S stream, warp 11 the PV stream (one
+    // thread issues a tcgen05.mma about every 64 cycles at best, and slower when busy warps share
+    // its sub-partition: two issuers keep the tensor core fed).  The streams touch disjoint TMEM
+    // (S buffers; P buffers and O) and are ordered only through the softmax's barriers.
     if (lane == 0) {
       constexpr bool kB = Elem<T>::kBf16;
       constexpr uint32_t idS = idesc_f16(kB, false, false, 128, kBN);
       constexpr uint32_t idO = idesc_f16(kB, false, true, 128, DP);
-      // Descriptors are built once; a k-step adds its byte offset >> 4 to the start-address
-      // field (shared addresses stay below 256 KB, so the 14-bit field never carries).
       const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV = smem_desc_sw128(smem_u32(sV), L::kChunkBytes, 1024);
+      const bool s_side = warp == 9;
       bool ok = true;
-      // Each group is a straight run of MMAs: one base per operand, compile-time offsets, no
-      // branch between two MMAs (a branch or per-MMA address arithmetic there halves the rate
-      // at which one thread can feed the tensor core).
-      auto issue_s = [&](uint32_t t, uint32_t qs) {
-        const uint64_t qx = dQ + ((qs * L::kTileBytes) >> 4);
-        const uint64_t kx = dK + (((t % SK) * L::kTileBytes) >> 4);
-        const uint32_t d = tmem + (t & 1) * 128;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < DP / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-          mma_ss(d, qx + off, kx + off, idS, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full + (t & 1));
-      };
-      auto issue_pv = [&](uint32_t t, bool first) {
-        tc_fence_after();
-        const uint64_t vx = dV + (((t % SV) * L::kTileBytes) >> 4);
-        // P(t) in P buffer t % 2: keys 2c, 2c+1 in column c
-        const uint32_t pa = tmem + L::kColP + (t & 1) * 64;
-        const uint32_t acc0 = first ? 0u : 1u;
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_ts(tmem + L::kColO, pa + ks * 8, vx + ((ks * 2048) >> 4), idO, ks > 0 ? 1u : acc0);
-        mma_commit(pv_done + (t & 1));
-        mma_commit(v_empty + t % SV);
-      };
-      // A small scheduler over the two streams of an item, polled without blocking:
-      //   S(j)  needs Q, K_j, and S(j-2) loaded by the softmax (S buffer j % 2 free);
-      //   PV(j) needs P(j) (p_full) and V_j, and for an item's first tile the previous item's O
-      //         read out (o_free).
-      // K_j is released once S(j) is issued, Q once the item's last S is.  Every barrier tested
-      // here cannot complete its next phase before this thread issues something, so a phase is
-      // never skipped between two polls.  (Letting S run on into the next item while the last
-      // PVs of this one are pending measured slower: those PVs gate the item's epilogue.)
       uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
       uint32_t ic = 0;
       for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
@@ -477,51 +448,57 @@ __global__ void __launch_bounds__(352, 1)
         const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
         if (!it.valid) continue;
         const int n = it.n_kv;
-        const uint32_t t0 = kv;
         const uint32_t qs = ic % SQ;
-        int ns = 0, np = 0;
-        bool q_ready = false;
-        unsigned long long t_idle = 0;
-        while (np < n) {
-          bool progress = false;
-          if (!q_ready) q_ready = mbar_test(q_full + qs, (ic / SQ) & 1);
-          const uint32_t ts = t0 + ns;
-          if (q_ready && ns < n && mbar_test(k_full + ts % SK, (ts / SK) & 1) &&
-              (ts < 2 || mbar_test(s_free + (ts & 1), ((ts - 2) >> 1) & 1))) {
-            issue_s(ts, qs);
-            mma_commit(k_empty + ts % SK);
-            ++ns;
-            if (ns == n && !tile_item(it)) mma_commit(q_empty + qs);
-            progress = true;
-          }
-          const uint32_t tp = t0 + np;
-          if (np < ns && mbar_test(p_full + (tp & 1), (tp >> 1) & 1) && mbar_test(v_full + tp % SV, (tp / SV) & 1) &&
-              (np > 0 || ic == 0 || mbar_test(o_free, (ic - 1) & 1))) {
-            issue_pv(tp, np == 0);
-            ++np;
-            progress = true;
-          }
-          if (progress) {
-            t_idle = 0;
-          } else {
-            const unsigned long long now = globaltimer();
-            if (t_idle == 0) t_idle = now;
-            if (abort_read(abort_flag)) { ok = false; break; }
-            if (now - t_idle > wait_limit(abort_flag)) {
-              raise_status(p.status, ATTN_ERR_TIMEOUT);
-              abort_set(abort_flag, 1);
+        if (s_side) {
+          if (!mbar_wait(q_full + qs, (ic / SQ) & 1, abort_flag, p.status)) { ok = false; break; }
+          for (int j = 0; j < n; ++j) {
+            const uint32_t t = kv + j;
+            if (!mbar_wait(k_full + t % SK, (t / SK) & 1, abort_flag, p.status) ||
+                (t >= 2 && !mbar_wait(s_free + (t & 1), ((t - 2) >> 1) & 1, abort_flag, p.status))) {
               ok = false;
               break;
             }
+            tc_fence_after();
+            const uint64_t qx = dQ + ((qs * L::kTileBytes) >> 4);
+            const uint64_t kx = dK + (((t % SK) * L::kTileBytes) >> 4);
+            const uint32_t d = tmem + (t & 1) * 128;
+#pragma unroll
+            for (int ks = 0; ks < DP / 16; ++ks) {
+              const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+              mma_ss(d, qx + off, kx + off, idS, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(s_full + (t & 1));
+            mma_commit(k_empty + t % SK);
+            if (j == n - 1 && !tile_item(it)) mma_commit(q_empty + qs);
+          }
+        } else {
+          for (int j = 0; j < n; ++j) {
+            const uint32_t t = kv + j;
+            if (!mbar_wait(p_full + (t & 1), (t >> 1) & 1, abort_flag, p.status) ||
+                !mbar_wait(v_full + t % SV, (t / SV) & 1, abort_flag, p.status) ||
+                (j == 0 && ic > 0 && !mbar_wait(o_free, (ic - 1) & 1, abort_flag, p.status))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t vx = dV + (((t % SV) * L::kTileBytes) >> 4);
+            // P(t) in P buffer t % 2: keys 2c, 2c+1 in column c
+            const uint32_t pa = tmem + L::kColP + (t & 1) * 64;
+            const uint32_t acc0 = j == 0 ? 0u : 1u;
+#pragma unroll
+            for (int ks = 0; ks < kBN / 16; ++ks)
+              mma_ts(tmem + L::kColO, pa + ks * 8, vx + ((ks * 2048) >> 4), idO, ks > 0 ? 1u : acc0);
+            mma_commit(pv_done + (t & 1));
+            mma_commit(v_empty + t % SV);
           }
         }
-        if (!ok) break;
-        kv = t0 + n;
+        kv += n;
         ++ic;
       }
       if (!ok) {
-        mma_commit(drain);  // every MMA issued so far completes before this arrives
-        mbar_drain(drain, 0);
+        uint64_t* dr = s_side ? drain : drain2;
+        mma_commit(dr);  // every MMA this thread issued completes before this arrives
+        mbar_drain(dr, 0);
       }
     }
     __syncwarp();
