@@ -25,10 +25,11 @@
 //             into dS^T (hi/lo, into shared memory).  The next tile's LSE and D are prefetched.
 //   WG2       moves dQ_t from TMEM through shared memory into the fp32 workspace (TMA tile
 //             reductions; in key-tile order when deterministic) and writes dK, dV at the end.
-//   WG3       warp 12: TMA producer and TMEM allocator; warp 13: MMA issuer.
-// MMA order per query tile: S^T, dP^T, dV (hi, lo), dK (hi, lo), dQ (hi, lo).  The next
-// tile's S^T waits only for dV to have read P^T; its dP^T waits for the dQ readout.  Q and dO
-// have separate ring slots, released after the last MMA that reads each (dK, dV).
+//   WG3       warp 12: TMA producer and TMEM allocator; warps 13 and 14: MMA issuers.
+// Two MMA streams: warp 13 issues S^T, dP^T, dV (hi, lo) per query tile, warp 14 dK (hi, lo)
+// then dQ (hi, lo) once dS is written.  The next tile's S^T waits only for dV to have read P^T
+// and for its Q; its dP^T waits for the dQ readout.  Q and dO have separate ring slots,
+// released after the last MMA that reads each (dK, dV).
 #pragma once
 #include "fwd_tc.cuh"
 
@@ -54,8 +55,8 @@ struct BwdLayout {
   static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
   // kv_full, q_full[QS], q_empty[QS], do_full[QS], do_empty[QS], s_full, dp_full, p_full,
   // dv_done, ds_full, dsl_free, stage_free, dq_full, dq_free, dkdv_done, rows_ready,
-  // stage_full, drain
-  static constexpr int kNumBars = 1 + 4 * kQStages + 13;
+  // stage_full, drain, drain2
+  static constexpr int kNumBars = 1 + 4 * kQStages + 14;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag, wait limit (u64)
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
@@ -135,7 +136,8 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* dkdv_done = dq_free + 1;
   uint64_t* rows_ready = dkdv_done + 1;  // the 128 row terms (LSE, D) of the current tile are in smem
   uint64_t* stage_full = rows_ready + 1;  // the read-out warps have staged the dQ tile
-  uint64_t* drain = stage_full + 1;
+  uint64_t* drain = stage_full + 1;   // abort path of issuer 13
+  uint64_t* drain2 = drain + 1;        // abort path of issuer 14
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
@@ -195,10 +197,11 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(stage_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 4);
-    mbar_init(dkdv_done, 1);
+    mbar_init(dkdv_done, 2);
     mbar_init(rows_ready, kEw / 32);
     mbar_init(stage_full, 4);
     mbar_init(drain, 1);
+    mbar_init(drain2, 1);
     abort_set(abort_flag, 0);
     wait_limit_set(abort_flag, p.wait_ns);
     mbar_init_fence();
@@ -247,8 +250,12 @@ __global__ void __launch_bounds__(512, 1)
         for (int it = max(0, ndo_issued - QS); it < ndo_issued; ++it)
           mbar_drain(do_full + it % QS, (it / QS) & 1);
       }
-    } else if (warp == 13 && lane == 0) {
-      // ============================================================== MMA issuer
+    } else if ((warp == 13 || warp == 14) && lane == 0) {
+      // ============================================================== MMA issuers
+      // warp 13: S^T(t), dP^T(t), dV(t); warp 14: dK(t), then dQ(t), once dS(t) is written.  One
+      // thread feeds the tensor core at most one 128 x 128 x 16 MMA per ~64 cycles, and slower
+      // when busy warps share its sub-partition; with two issuers S^T(t+1) goes in as soon as
+      // Q(t+1) has landed instead of behind the issue of dQ(t).
       constexpr bool kB = Elem<T>::kBf16;
       constexpr uint32_t idSS = idesc_f16(kB, false, false, 128, 128);  // S^T, dP^T
       constexpr uint32_t idKD = idesc_f16(kB, false, true, 128, DP);    // dV, dK: B MN-major
@@ -270,81 +277,86 @@ __global__ void __launch_bounds__(512, 1)
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % QS;
         const uint32_t ph = (it / QS) & 1;
-        // ---- S^T = K Q^T (needs Q and the S columns: dV of the previous tile has read P^T)
-        if (!mbar_wait(q_full + st, ph, abort_flag, p.status)) { ok = false; break; }
-        if (it >= 1 && !mbar_wait(dv_done, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        {
-          const uint64_t a = opaque(dK_k), bq = opaque(dQ_k + st * kStage16);
+        if (warp == 13) {
+          // ---- S^T = K Q^T (needs Q and the S columns: dV of the previous tile has read P^T)
+          if (!mbar_wait(q_full + st, ph, abort_flag, p.status)) { ok = false; break; }
+          if (it >= 1 && !mbar_wait(dv_done, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const uint64_t a = opaque(dK_k), bq = opaque(dQ_k + st * kStage16);
 #pragma unroll
-          for (int ks = 0; ks < DP / 16; ++ks) {
-            const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-            mma_ss(tmem + L::kColS, a + off, bq + off, idSS, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < DP / 16; ++ks) {
+              const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+              mma_ss(tmem + L::kColS, a + off, bq + off, idSS, ks > 0 ? 1u : 0u);
+            }
           }
-        }
-        mma_commit(s_full);
-        // ---- dP^T = V dO^T (needs dO and the dP columns: dQ of the previous tile read out)
-        if (!mbar_wait(do_full + st, ph, abort_flag, p.status)) { ok = false; break; }
-        if (it >= 1 && !mbar_wait(dq_free, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        {
-          const uint64_t a = opaque(dV_k), bo = opaque(ddO_k + st * kStage16);
+          mma_commit(s_full);
+          // ---- dP^T = V dO^T (needs dO and the dP columns: dQ of the previous tile read out,
+          // which also means its dK and dQ MMAs have completed)
+          if (!mbar_wait(do_full + st, ph, abort_flag, p.status)) { ok = false; break; }
+          if (it >= 1 && !mbar_wait(dq_free, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const uint64_t a = opaque(dV_k), bo = opaque(ddO_k + st * kStage16);
 #pragma unroll
-          for (int ks = 0; ks < DP / 16; ++ks) {
-            const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-            mma_ss(tmem + L::kColdP, a + off, bo + off, idSS, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < DP / 16; ++ks) {
+              const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+              mma_ss(tmem + L::kColdP, a + off, bo + off, idSS, ks > 0 ? 1u : 0u);
+            }
           }
-        }
-        mma_commit(dp_full);
-        // ---- dV += P^T dO; P^T hi/lo in TMEM: the 16 queries of k-step ks sit in the 32-column
-        // group ks/2 (hi in its first 16 columns, lo in the last 16), 8 columns per k-step
-        if (!mbar_wait(p_full, it & 1, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        {
-          const uint64_t bo = opaque(ddO_mn + st * kStage16);
-          const uint32_t acc0 = it > 0 ? 1u : 0u;
+          mma_commit(dp_full);
+          // ---- dV += P^T dO; P^T hi/lo in TMEM: the 16 queries of k-step ks sit in the 32-column
+          // group ks/2 (hi in its first 16 columns, lo in the last 16), 8 columns per k-step
+          if (!mbar_wait(p_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const uint64_t bo = opaque(ddO_mn + st * kStage16);
+            const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks) {
-            const uint32_t acol = L::kColS + (ks >> 1) * 32 + (ks & 1) * 8;
-            const uint64_t bd = bo + ((ks * 2048) >> 4);
-            mma_ts(tmem + L::kColdV, tmem + acol, bd, idKD, ks > 0 ? 1u : acc0);
-            mma_ts(tmem + L::kColdV, tmem + acol + 16, bd, idKD, 1u);
+            for (int ks = 0; ks < kBN / 16; ++ks) {
+              const uint32_t acol = L::kColS + (ks >> 1) * 32 + (ks & 1) * 8;
+              const uint64_t bd = bo + ((ks * 2048) >> 4);
+              mma_ts(tmem + L::kColdV, tmem + acol, bd, idKD, ks > 0 ? 1u : acc0);
+              mma_ts(tmem + L::kColdV, tmem + acol + 16, bd, idKD, 1u);
+            }
           }
-        }
-        mma_commit(dv_done);
-        mma_commit(do_empty + st);
-        // ---- dK += dS^T Q (hi, lo)
-        if (!mbar_wait(ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        {
-          const uint64_t ah = opaque(dSh_k), al = opaque(dSl_k), bq = opaque(dQ_mn + st * kStage16);
-          const uint32_t acc0 = it > 0 ? 1u : 0u;
+          mma_commit(dv_done);
+          mma_commit(do_empty + st);
+        } else {
+          // ---- dK += dS^T Q (hi, lo)
+          if (!mbar_wait(ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const uint64_t ah = opaque(dSh_k), al = opaque(dSl_k), bq = opaque(dQ_mn + st * kStage16);
+            const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks) {
-            const uint32_t a_off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-            const uint64_t bd = bq + ((ks * 2048) >> 4);
-            mma_ss(tmem + L::kColdK, ah + a_off, bd, idKD, ks > 0 ? 1u : acc0);
-            mma_ss(tmem + L::kColdK, al + a_off, bd, idKD, 1u);
+            for (int ks = 0; ks < kBN / 16; ++ks) {
+              const uint32_t a_off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+              const uint64_t bd = bq + ((ks * 2048) >> 4);
+              mma_ss(tmem + L::kColdK, ah + a_off, bd, idKD, ks > 0 ? 1u : acc0);
+              mma_ss(tmem + L::kColdK, al + a_off, bd, idKD, 1u);
+            }
           }
-        }
-        mma_commit(q_empty + st);
-        // ---- dQ_t = dS K (hi, lo), dS read MN-major from the dS^T tiles, into the dP columns
-        {
-          const uint64_t ah = opaque(dSh_mn), al = opaque(dSl_mn), bk = opaque(dK_mn);
+          mma_commit(q_empty + st);
+          // ---- dQ_t = dS K (hi, lo), dS read MN-major from the dS^T tiles, into the dP columns
+          {
+            const uint64_t ah = opaque(dSh_mn), al = opaque(dSl_mn), bk = opaque(dK_mn);
 #pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks) {
-            const uint32_t off = (ks * 2048) >> 4;
-            mma_ss(tmem + L::kColdQ, ah + off, bk + off, idQ, ks > 0 ? 1u : 0u);
-            mma_ss(tmem + L::kColdQ, al + off, bk + off, idQ, 1u);
+            for (int ks = 0; ks < kBN / 16; ++ks) {
+              const uint32_t off = (ks * 2048) >> 4;
+              mma_ss(tmem + L::kColdQ, ah + off, bk + off, idQ, ks > 0 ? 1u : 0u);
+              mma_ss(tmem + L::kColdQ, al + off, bk + off, idQ, 1u);
+            }
           }
+          mma_commit(dq_full);
         }
-        mma_commit(dq_full);
       }
+      uint64_t* dr = warp == 13 ? drain : drain2;
       if (ok) {
-        mma_commit(dkdv_done);
+        mma_commit(dkdv_done);  // one commit from each issuer after its last MMA
       } else {
-        mma_commit(drain);
-        mbar_drain(drain, 0);
+        mma_commit(dr);
+        mbar_drain(dr, 0);
       }
     }
     __syncwarp();
