@@ -77,16 +77,21 @@ __device__ __forceinline__ void split_pack(float a, float b, uint32_t& hi, uint3
 template <>
 __device__ __forceinline__ void split_pack<__nv_bfloat16>(float a, float b, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
+  const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h);
+  // hi back in fp32 (a bf16 is the top half of an fp32), then x - hi for both with one paired
+  // FMA; the difference is exact
+  const uint64_t hf = f2_pack(__uint_as_float(hb << 16), __uint_as_float(hb & 0xffff0000u));
+  const float2 r = f2_unpack(f2_fma(hf, f2_pack(-1.f, -1.f), f2_pack(a, b)));
+  const __nv_bfloat162 l = __floats2bfloat162_rn(r.x, r.y);
+  hi = hb;
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 template <>
 __device__ __forceinline__ void split_pack<__half>(float a, float b, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(a, b);
   const float2 hf = __half22float2(h);
-  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  const float2 r = f2_unpack(f2_fma(f2_pack(hf.x, hf.y), f2_pack(-1.f, -1.f), f2_pack(a, b)));
+  const __half2 l = __floats2half2_rn(r.x, r.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
