@@ -16,22 +16,23 @@
 // A CTA loops over 128-row query tiles, numbered heaviest first under the causal mask and
 // dealt to the CTAs in snake order (cta_item).  384 threads:
 //   warps 0-3  softmax, key columns 0-63 of each S tile; warps 4-7 softmax, key columns 64-127.
-//              Thread t of either group owns query row t (TMEM lane t).  The two threads of a
-//              row exchange their partial row maxima through shared memory, so both use the
-//              same running max; each keeps its own partial row sum, combined at the end.  Each
-//              writes its 64 P values (16-bit pairs) into its 32 columns of the P buffer,
-//              rescales its half of the O row when the max moved, and at the end normalises
-//              that half of O: into the item's Q slot for a tile store, or to global memory.
+//              Thread t of either group owns query row t (TMEM lane t).  Each group keeps its
+//              own running max and sum over its key columns and its own O accumulator (O_g =
+//              sum of P_g V over those keys), so the two never wait for each other inside an
+//              item.  Each writes its 64 P values (16-bit pairs) over the first 32 of its S
+//              columns and rescales O_g when its max moved.  At the end of the item the two
+//              threads of a row exchange (max, sum), and each writes half of the row of
+//              O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l: into the item's Q slot for a tile
+//              store, or to global memory.
 //   warp 8     TMA producer (lane 0) and TMEM allocator (whole warp).
 //   warp 9     MMA issuer of the S(j) stream (lane 0).
 //   warp 10    output tile stores (lane 0): writes each staged O tile with TMA and frees the
 //              Q slot.
 //   warp 11    MMA issuer of the PV(j) stream (lane 0).
-// TMEM: S double buffer at columns [0,128) and [128,256), P double buffer (16-bit pairs) at
-// [256,320) and [320,384), O at [384, 384+DP).  S(j) goes into S buffer j % 2 as soon as the
-// softmax has loaded S(j-2) into registers, and P(j) into P buffer j % 2 once PV(j-2) has read
-// P(j-2): no MMA waits for another MMA, and the tensor core computes S(j+1) (and S(j+2)) while
-// the softmax works on S(j).
+// TMEM: S double buffer at columns [0,128) and [128,256), P(j) of group g over columns
+// [64g, 64g+32) of S buffer j % 2, O_0 at [256, 256+DP) and O_1 after it.  S(j+2) goes into S
+// buffer j % 2 once PV(j) has read P(j), so the tensor core computes S(j+1) while the softmax
+// works on S(j).
 //
 // Lazy rescaling: the running max used for the exponentials is only moved when a tile's max
 // exceeds it by more than kRescaleLog2 (log2 units); the final O / l and LSE use the same max,
@@ -90,7 +91,7 @@ struct FwdLayout {
   static constexpr int kOffX = kOffV + kStagesV * kTileBytes;  // exchange [2 slots][2 groups][128 rows]
   static constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
   // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
-  // s_free[2], p_full[2], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain,
+  // p_full[2 buffers][2 groups], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain,
   // o_staged[2] (per Q slot, so it cannot run two phases ahead of the store warp: a slot takes
   // a new Q only after the store warp has written out the tile staged in it), drain2
   static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1 + 2 + 1;
@@ -99,7 +100,7 @@ struct FwdLayout {
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColP = 256, kColO = 384;
+  static constexpr uint32_t kColO = 256;  // O_0; O_1 at kColO + DP
   static constexpr int kThreads = 384;
 };
 
@@ -276,12 +277,11 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* k_empty = k_full + SK;
   uint64_t* v_full = k_empty + SK;
   uint64_t* v_empty = v_full + SV;
-  // Per buffer b: s_full (S(j) ready), s_free (S(j) loaded by the softmax), p_full (P(j)
-  // written), pv_done (PV(j) done), for the tiles j with j % 2 == b; phase k is tile 2k + b.
+  // Per buffer b: s_full (S(j) ready), p_full[b * 2 + g] (group g has written P(j)), pv_done
+  // (PV(j) of both groups done), for the tiles j with j % 2 == b; phase k is tile 2k + b.
   uint64_t* s_full = v_empty + SV;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 2;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 4;
   uint64_t* o_free = pv_done + 2;
   uint64_t* xch = o_free + 1;       // [quadrant][slot]: row-max / row-sum exchange, warps q and q + 4
   uint64_t* drain = xch + 8;
@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(s_free + i, 8);  // one arrival per softmax warp
-      mbar_init(p_full + i, 8);
+      mbar_init(p_full + 2 * i, 4);  // one arrival per softmax warp of the group
+      mbar_init(p_full + 2 * i + 1, 4);
       mbar_init(pv_done + i, 1);
     }
     mbar_init(o_free, 8);
@@ -453,8 +453,9 @@ __global__ void __launch_bounds__(384, 1)
           if (!mbar_wait(q_full + qs, (ic / SQ) & 1, abort_flag, p.status)) { ok = false; break; }
           for (int j = 0; j < n; ++j) {
             const uint32_t t = kv + j;
+            // S buffer t % 2 holds P(t-2) until PV(t-2) has read it
             if (!mbar_wait(k_full + t % SK, (t / SK) & 1, abort_flag, p.status) ||
-                (t >= 2 && !mbar_wait(s_free + (t & 1), ((t - 2) >> 1) & 1, abort_flag, p.status))) {
+                (t >= 2 && !mbar_wait(pv_done + (t & 1), ((t - 2) >> 1) & 1, abort_flag, p.status))) {
               ok = false;
               break;
             }
@@ -474,21 +475,28 @@ __global__ void __launch_bounds__(384, 1)
         } else {
           for (int j = 0; j < n; ++j) {
             const uint32_t t = kv + j;
-            if (!mbar_wait(p_full + (t & 1), (t >> 1) & 1, abort_flag, p.status) ||
-                !mbar_wait(v_full + t % SV, (t / SV) & 1, abort_flag, p.status) ||
+            const uint32_t b = t & 1;
+            if (!mbar_wait(v_full + t % SV, (t / SV) & 1, abort_flag, p.status) ||
                 (j == 0 && ic > 0 && !mbar_wait(o_free, (ic - 1) & 1, abort_flag, p.status))) {
               ok = false;
               break;
             }
-            tc_fence_after();
             const uint64_t vx = dV + (((t % SV) * L::kTileBytes) >> 4);
-            // P(t) in P buffer t % 2: keys 2c, 2c+1 in column c
-            const uint32_t pa = tmem + L::kColP + (t & 1) * 64;
             const uint32_t acc0 = j == 0 ? 0u : 1u;
+            // PV_g(t): O_g (+)= P_g(t) V[64g, 64g + 64), P_g over the first 32 columns of group
+            // g's half of S buffer b (keys 2c, 2c+1 in column c)
 #pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks)
-              mma_ts(tmem + L::kColO, pa + ks * 8, vx + ((ks * 2048) >> 4), idO, ks > 0 ? 1u : acc0);
-            mma_commit(pv_done + (t & 1));
+            for (int g = 0; g < 2; ++g) {
+              if (!mbar_wait(p_full + 2 * b + g, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t pa = tmem + b * 128 + g * 64;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                mma_ts(tmem + L::kColO + g * DP, pa + ks * 8, vx + (((4 * g + ks) * 2048) >> 4), idO,
+                       ks > 0 ? 1u : acc0);
+            }
+            if (!ok) break;
+            mma_commit(pv_done + b);
             mma_commit(v_empty + t % SV);
           }
         }
@@ -534,7 +542,7 @@ __global__ void __launch_bounds__(384, 1)
     const int grp = warp >> 2;                // 0: key columns 0-63, 1: key columns 64-127
     const int row = threadIdx.x & 127;        // TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t tO = tl + L::kColO + grp * (DP / 2);  // this group's half of the O row
+    const uint32_t tOg = tl + L::kColO + grp * DP;  // this group's accumulator O_g
     const float sl2 = p.scale_log2;
     uint32_t kv = 0, ic = 0;
     uint32_t xc = 0;  // exchanges done (slot xc % 2, phase (xc / 2) % 2)
@@ -563,18 +571,18 @@ __global__ void __launch_bounds__(384, 1)
         last_key = CAUSAL ? min(q_row % p.Nq + it.seq_len - p.Nq, it.seq_len - 1) : it.seq_len - 1;
       else
         last_key = CAUSAL ? min(q_row, it.seq_len - 1) : it.seq_len - 1;
-      float m = -INFINITY, l = 0.f;          // l: this group's partial row sum
+      float m = -INFINITY, l = 0.f;  // this group's running max (log2 units) and sum
       for (int j = 0; j < it.n_kv; ++j) {
         const uint32_t t = kv + j;
         const int b = t & 1;
         if (!mbar_wait_warp(s_full + b, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tS = tl + b * 128;
+        const uint32_t tS = tl + b * 128 + grp * 64;  // this group's 64 columns of S buffer b
         float s[64];
         {
           uint32_t r0[32], r1[32];
-          tmem_ld32(tS + grp * 64, r0);
-          tmem_ld32(tS + grp * 64 + 32, r1);
+          tmem_ld32(tS, r0);
+          tmem_ld32(tS + 32, r1);
           tmem_ld_wait();
           tmem_reg_fence(r0);
           tmem_reg_fence(r1);
@@ -584,8 +592,6 @@ __global__ void __launch_bounds__(384, 1)
             s[32 + i] = __uint_as_float(r1[i]);
           }
         }
-        tc_fence_before();
-        mbar_arrive_warp(s_free + b);  // S buffer b may take S(t+2)
         // keys key0 + c with c > lim are masked (past the diagonal, or past the sequence)
         const int key0 = (it.j0 + j) * kBN + grp * 64;
         const int lim = last_key - key0;
@@ -593,7 +599,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) s[c] = c > lim ? -INFINITY : s[c];
         }
-        // partial row max (3-input max, 4 chains), then the other group's
+        // row max over this group's columns (3-input max, 4 chains)
         float m0 = max3f(s[0], s[1], s[2]), m1 = max3f(s[3], s[4], s[5]);
         float m2 = max3f(s[6], s[7], s[8]), m3 = max3f(s[9], s[10], s[11]);
 #pragma unroll
@@ -605,11 +611,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         m0 = max3f(m0, s[60], s[61]);
         m1 = max3f(m1, s[62], s[63]);
-        float mx = max3f(m0, m1, fmaxf(m2, m3));
-        float mo;
-        if (!exchange(mx, mo)) { ok = false; break; }
-        mx = fmaxf(mx, mo);
-        const float mx2 = mx * sl2;  // scale > 0: max commutes with the scaling
+        const float mx2 = max3f(m0, m1, fmaxf(m2, m3)) * sl2;  // scale > 0: max commutes with it
         float alpha = 1.f;
         bool resc = false;
         if (mx2 > m + kRescaleLog2 || (m == -INFINITY && mx2 != -INFINITY)) {
@@ -651,13 +653,11 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         const float2 rs2 = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
-        const float rs = rs2.x + rs2.y;
-        l = l * alpha + rs;
-        // P over this group's 32 columns of P buffer b, free once PV(t-2) has read P(t-2)
-        if (t >= 2 && !mbar_wait_warp(pv_done + b, ((t >> 1) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        tmem_st32(tl + L::kColP + b * 64 + grp * 32, pk);
-        // O half-row *= alpha: O must hold PV(t-1) first, so wait for it (only when rescaling)
+        l = l * alpha + (rs2.x + rs2.y);
+        // P over the first 32 of this group's S columns, already in registers; the S buffer takes
+        // S(t+2) only after PV(t) has read P
+        tmem_st32(tS, pk);
+        // O_g *= alpha: O_g must hold PV(t-1) first, so wait for it (only when rescaling)
         if (__any_sync(0xffffffffu, resc)) {
           if (t > 0 && !mbar_wait_warp(pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, p.status)) {
             ok = false;
@@ -667,30 +667,35 @@ __global__ void __launch_bounds__(384, 1)
           const float a = resc ? alpha : 1.f;
           uint32_t r[32];
 #pragma unroll
-          for (int c = 0; c < DP / 64; ++c) {
-            tmem_ld32(tO + c * 32, r);
+          for (int c = 0; c < DP / 32; ++c) {
+            tmem_ld32(tOg + c * 32, r);
             tmem_ld_wait();
             tmem_reg_fence(r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
-            tmem_st32(tO + c * 32, r);
+            tmem_st32(tOg + c * 32, r);
           }
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive_warp(p_full + b);
+        mbar_arrive_warp(p_full + 2 * b + grp);
       }
       if (!ok) break;
       kv += it.n_kv;
-      // ---- epilogue: combine the two partial row sums, O / l and LSE
-      float lo;
-      if (!exchange(l, lo)) { ok = false; break; }
-      const float l_all = l + lo;
+      // ---- epilogue: the row's max and sum from both groups; O = (O_0 a_0 + O_1 a_1) / l
+      float mo, lo;
+      if (!exchange(m, mo) || !exchange(l, lo)) { ok = false; break; }
+      const float mr = fmaxf(m, mo);
+      const float a_self = (m == -INFINITY) ? 0.f : ex2_approx(m - mr);
+      const float a_other = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mr);
+      const float l_all = l * a_self + lo * a_other;
       const uint32_t tl_last = kv - 1;
       if (!mbar_wait_warp(pv_done + (tl_last & 1), (tl_last >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       const bool valid = q_row < (KV ? p.R : it.seq_len);
       const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
+      // weights of O_0 and O_1 in this row's output
+      const float c0 = (grp == 0 ? a_self : a_other) * inv_l, c1 = (grp == 0 ? a_other : a_self) * inv_l;
       size_t row_off;
       // a KV cache range writes its partial output in fp32 to its slice of the split buffer
       const size_t kv_row = KV ? (static_cast<size_t>(it.split) * p.B * p.Hkv + static_cast<size_t>(it.b) * p.Hkv + it.h) * p.R + q_row : 0;
@@ -702,77 +707,74 @@ __global__ void __launch_bounds__(384, 1)
         row_off = ((static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row) * p.d;
       const bool o_f32 = KV || p.out_f32;
       void* const o_base = KV ? static_cast<void*>(p.o_part) : p.o;
-      uint32_t r[32];
       const bool tile = tile_item(it);
-      if (tile) {
-        // this group's DP / 2 columns of row `row` (from column grp * DP / 2) into the item's Q
-        // slot, in the 128-byte swizzled layout of the output map's {64, 128} boxes: column
-        // col lands in box col / 64, 16-byte granule (col % 64) / 8; rows and columns past the
-        // tensor are clipped by the store
-        constexpr int kHalf = DP / 2;
-        uint8_t* srow = sQ + (ic % SQ) * L::kTileBytes + ((grp * kHalf) / 64) * L::kChunkBytes + row * 128;
-        const int gran0 = ((grp * kHalf) % 64) / 8;
+      // this thread's DP / 2 output columns, from column grp * DP / 2, 32 at a time: both
+      // accumulators loaded, combined in registers
+      constexpr int kHalf = DP / 2;
+      const uint32_t tO0 = tl + L::kColO + grp * kHalf, tO1 = tO0 + DP;
+      uint8_t* srow = sQ + (ic % SQ) * L::kTileBytes + ((grp * kHalf) / 64) * L::kChunkBytes + row * 128;
+      const int gran0 = ((grp * kHalf) % 64) / 8;
 #pragma unroll
-        for (int c = 0; c < DP / 64; ++c) {
-          tmem_ld32(tO + c * 32, r);
-          tmem_ld_wait();
-          tmem_reg_fence(r);
-          if (c == DP / 64 - 1) {
-            tc_fence_before();
-            mbar_arrive_warp(o_free);  // O is in registers: the next item may overwrite it
-          }
+      for (int c = 0; c < DP / 64; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tO0 + c * 32, r0);
+        tmem_ld32(tO1 + c * 32, r1);
+        tmem_ld_wait();
+        tmem_reg_fence(r0);
+        tmem_reg_fence(r1);
+        if (c == DP / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive_warp(o_free);  // both accumulators are in registers: the next item may overwrite them
+        }
+        float o[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r0[i]) * c0 + __uint_as_float(r1[i]) * c1;
+        if (tile) {
+          // into the item's Q slot, in the 128-byte swizzled layout of the output map's {64, 128}
+          // boxes: column col lands in box col / 64, 16-byte granule (col % 64) / 8; rows and
+          // columns past the tensor are clipped by the store
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 v;
-            v.x = Elem<T>::pack(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
-            v.y = Elem<T>::pack(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
-            v.z = Elem<T>::pack(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
-            v.w = Elem<T>::pack(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+            v.x = Elem<T>::pack(o[8 * i + 0], o[8 * i + 1]);
+            v.y = Elem<T>::pack(o[8 * i + 2], o[8 * i + 3]);
+            v.z = Elem<T>::pack(o[8 * i + 4], o[8 * i + 5]);
+            v.w = Elem<T>::pack(o[8 * i + 6], o[8 * i + 7]);
             const int gran = gran0 + c * 4 + i;
             *reinterpret_cast<uint4*>(srow + ((gran ^ (row & 7)) << 4)) = v;
           }
-        }
-        fence_async_smem();
-        mbar_arrive_warp(o_staged + ic % SQ);
-      }
+        } else {
+          const int col0 = grp * kHalf + c * 32;
+          if (valid && col0 < p.d) {
+            const int ncol = min(32, p.d - col0);  // 16 or 32 (d is a multiple of 16)
+            if (o_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o_base) + row_off + col0);
 #pragma unroll
-      for (int c = 0; c < (tile ? 0 : DP / 64); ++c) {
-        tmem_ld32(tO + c * 32, r);
-        tmem_ld_wait();
-        tmem_reg_fence(r);
-        const int col0 = grp * (DP / 2) + c * 32;
-        if (valid && col0 < p.d) {
-          const int ncol = min(32, p.d - col0);  // 16 or 32 (d is a multiple of 16)
-          if (o_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o_base) + row_off + col0);
+              for (int i = 0; i < 8; ++i)
+                if (i * 4 < ncol) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(o_base) + row_off + col0);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (i * 4 < ncol)
-                dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
-                                     __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
-            }
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(o_base) + row_off + col0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (i * 8 < ncol) {
-                uint4 v;
-                v.x = Elem<T>::pack(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
-                v.y = Elem<T>::pack(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
-                v.z = Elem<T>::pack(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
-                v.w = Elem<T>::pack(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
-                dst[i] = v;
+              for (int i = 0; i < 4; ++i) {
+                if (i * 8 < ncol) {
+                  uint4 v;
+                  v.x = Elem<T>::pack(o[8 * i + 0], o[8 * i + 1]);
+                  v.y = Elem<T>::pack(o[8 * i + 2], o[8 * i + 3]);
+                  v.z = Elem<T>::pack(o[8 * i + 4], o[8 * i + 5]);
+                  v.w = Elem<T>::pack(o[8 * i + 6], o[8 * i + 7]);
+                  dst[i] = v;
+                }
               }
             }
           }
         }
       }
-      if (!tile) {
-        tc_fence_before();
-        mbar_arrive_warp(o_free);
+      if (tile) {
+        fence_async_smem();
+        mbar_arrive_warp(o_staged + ic % SQ);
       }
       if (grp == 0 && valid && (KV || p.lse)) {
-        const float lse = (m + __log2f(l_all)) * 0.69314718055994531f;
+        const float lse = (mr + __log2f(l_all)) * 0.69314718055994531f;
         if constexpr (KV)
           p.lse_part[kv_row] = lse;
         else if constexpr (VARLEN)
