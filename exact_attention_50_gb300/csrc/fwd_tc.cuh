@@ -67,8 +67,8 @@ struct Elem<__half> {
 constexpr float kRescaleLog2 = 8.0f;
 // Which of every 8 exponential pairs run on the FMA pipe (bit k: pair k) instead of the
 // special-function unit.  None: at 32 results per clock per SM the special-function unit keeps
-// up with the MMAs, and the polynomial's extra instructions cost more issue slots than they
-// save (measured with 1/2, 1/4, 1/8 and none of the pairs on the FMA pipe: none is fastest).
+// up with the MMAs, and the polynomial's extra instructions cost about as many issue slots as
+// they save (1/8 of the pairs on the FMA pipe measured within +-1%, 1/4 and 1/2 slower).
 constexpr unsigned kPolyPairs = 0x00u;
 
 template <int DP, int MODE>
