@@ -586,12 +586,18 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device status after timed region: {_lib.status_string(st)}")
     value = replica_throughput(step_flops, world, ms_step)
 
-    # end to end: pinned host inputs in, results out, inside the timed region
+    # end to end: pinned host inputs in, results out, inside the timed region.  Two forms, both
+    # through the same calls: serial (copy in, step, copy out, one stream) and pipelined (two
+    # sets of device buffers; step i's inputs go up on one copy stream and step i-1's results
+    # come down on another while step i-1 / i compute, ordered by per-step events).  Every step
+    # still moves its own inputs and results across the link inside the timed region.
     e2e = None
     if not args.no_e2e:
         hin = [t.pin_memory() for t in S.host_in]
         hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in S.dev_out]
         Ke = args.e2e_steps or max(3, min(K, 50))
+        h2d_bytes = int(sum(t.numel() * t.element_size() for t in hin))
+        d2h_bytes = int(sum(t.numel() * t.element_size() for t in hout))
 
         def e2e_step():
             for h, d_ in zip(hin, S.dev_in):
@@ -611,11 +617,62 @@ def run_ours(args, rank, world, local):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ms_e = max_over_ranks(e0.elapsed_time(e1), world)
-        e2e = {"value": replica_throughput(step_flops, world, ms_e / Ke), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hin)),
-               "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hout)),
-               "ms_per_step": ms_e / Ke, "steps": Ke}
+        ms_serial = max_over_ranks(e0.elapsed_time(e1), world) / Ke
+
+        # pipelined: a second buffer set, an upload and a download stream
+        S2 = setup_step(wl, dev, lib, sp, bwd_flags)
+        sets = [S, S2]
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        up_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        down_done = [torch.cuda.Event() for _ in range(2)]
+
+        def pipelined(n, t_start=None, t_end=None):
+            for i in range(n):
+                k = i % 2
+                St = sets[k]
+                with torch.cuda.stream(up):
+                    if i == 0 and t_start is not None:
+                        t_start.record(up)
+                    if i >= 2:
+                        up.wait_event(comp_done[k])  # step i-2 has read this set's inputs
+                    for h, d_ in zip(hin, St.dev_in):
+                        d_.copy_(h, non_blocking=True)
+                    up_done[k].record(up)
+                stream.wait_event(up_done[k])
+                if i >= 2:
+                    stream.wait_event(down_done[k])  # step i-2's results have left this set
+                run_step(St, stream)
+                comp_done[k].record(stream)
+                with torch.cuda.stream(down):
+                    down.wait_event(comp_done[k])
+                    for h, d_ in zip(hout, St.dev_out):
+                        h.copy_(d_, non_blocking=True)
+                    down_done[k].record(down)
+            if t_end is not None:
+                # the timed region ends when the last download is done (every upload and step
+                # precede it)
+                stream.wait_event(down_done[(n - 1) % 2])
+                t_end.record(stream)
+
+        pipelined(4)
+        torch.cuda.synchronize()
+        barrier()
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        pipelined(Ke, p0, p1)
+        torch.cuda.synchronize()
+        barrier()
+        ms_pipe = max_over_ranks(p0.elapsed_time(p1), world) / Ke
+        st = lib.attn_get_device_status(sp)
+        if st != 0:
+            raise RuntimeError(f"device status after the end-to-end runs: {_lib.status_string(st)}")
+        e2e = {"value": replica_throughput(step_flops, world, ms_pipe), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+               "ms_per_step": ms_pipe, "steps": Ke,
+               "mode": "pipelined: two device buffer sets, uploads and downloads on their own streams",
+               "serial": {"value": replica_throughput(step_flops, world, ms_serial), "ms_per_step": ms_serial}}
+        del S2
 
     peaks = read_peaks()
     sm_count = props.multi_processor_count
