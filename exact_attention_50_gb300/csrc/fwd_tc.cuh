@@ -14,21 +14,24 @@
 // mask are applied inside the GEMM loop as in its best practice 2.
 //
 // A CTA loops over 128-row query tiles, numbered heaviest first under the causal mask and
-// dealt to the CTAs in snake order (cta_item).  384 threads:
+// dealt to the CTAs in snake order (cta_item).  512 threads:
 //   warps 0-3  softmax, key columns 0-63 of each S tile; warps 4-7 softmax, key columns 64-127.
 //              Thread t of either group owns query row t (TMEM lane t).  Each group keeps its
 //              own running max and sum over its key columns and its own O accumulator (O_g =
 //              sum of P_g V over those keys), so the two never wait for each other inside an
 //              item.  Each writes its 64 P values (16-bit pairs) over the first 32 of its S
-//              columns and rescales O_g when its max moved.  At the end of the item the two
-//              threads of a row exchange (max, sum), and each writes half of the row of
-//              O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l: into the item's Q slot for a tile
-//              store, or to global memory.
+//              columns and rescales O_g when its max moved.  At the end of the item each
+//              hands its (max, sum) to the epilogue warps and goes on to the next item.
 //   warp 8     TMA producer (lane 0) and TMEM allocator (whole warp).
 //   warp 9     MMA issuer of the S(j) stream (lane 0).
 //   warp 10    output tile stores (lane 0): writes each staged O tile with TMA and frees the
 //              Q slot.
 //   warp 11    MMA issuer of the PV(j) stream (lane 0).
+//   warps 12-15 epilogue: per item, once its last PV has completed, combine O_0 and O_1 with
+//              the two groups' (max, sum) into O / l and LSE, staged for the tile stores or
+//              stored per row, while the softmax warps already work on the next item.
+// Registers: launched at 128 per thread, then split per warpgroup with setmaxnreg (softmax
+// 168, I/O 56, epilogue 120).
 // TMEM: S double buffer at columns [0,128) and [128,256), P(j) of group g over columns
 // [64g, 64g+32) of S buffer j % 2, O_0 at [256, 256+DP) and O_1 after it.  S(j+2) goes into S
 // buffer j % 2 once PV(j) has read P(j), so the tensor core computes S(j+1) while the softmax
@@ -88,20 +91,25 @@ struct FwdLayout {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kStagesQ * kTileBytes;
   static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
-  static constexpr int kOffX = kOffV + kStagesV * kTileBytes;  // exchange [2 slots][2 groups][128 rows]
+  static constexpr int kOffX = kOffV + kStagesV * kTileBytes;  // item end (m, l): [2 groups][128 rows]
   static constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
   // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
-  // p_full[2 buffers][2 groups], pv_done[2], o_free, xch[4 row quadrants][2 slots], drain,
+  // p_full[2 buffers][2 groups], pv_done[2], o_free, drain,
   // o_staged[2] (per Q slot, so it cannot run two phases ahead of the store warp: a slot takes
-  // a new Q only after the store warp has written out the tile staged in it), drain2
-  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 2 + 1 + 8 + 1 + 2 + 1;
+  // a new Q only after the store warp has written out the tile staged in it), drain2,
+  // stats_ready, stats_free
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 4 + 2 + 1 + 1 + 2 + 1 + 2;
   // tmem base (u32), abort flag (int), wait limit (u64, ns)
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;  // O_0; O_1 at kColO + DP
-  static constexpr int kThreads = 384;
+  static constexpr int kThreads = 512;
+  // launch 128 registers per thread; two softmax warpgroups at 168, the I/O warpgroup (producer,
+  // MMA issuers, tile stores) at 56 and the epilogue warpgroup at 120: 2 * 168 + 56 + 120 = 4 * 128
+  static constexpr uint32_t kLaunchRegs = 128, kRegsSmx = 168, kRegsIo = 56, kRegsEpi = 120;
+  static_assert(2 * kRegsSmx + kRegsIo + kRegsEpi == 4 * kLaunchRegs, "register split must match the launch");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -239,7 +247,7 @@ struct TileCursor {
 };
 
 template <typename T, int DP, bool CAUSAL, int MODE>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdParams p, int n_items) {
@@ -269,7 +277,8 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sQ = smem + L::kOffQ;
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
-  float* sX = reinterpret_cast<float*>(smem + L::kOffX);  // [slot][group][row]
+  // each group's running max and sum per row at the end of an item: [group][row] (m, l)
+  float2* sStats = reinterpret_cast<float2*>(smem + L::kOffX);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* q_full = bars;       // [2]: item i uses Q slot i % SQ
   uint64_t* q_empty = bars + 2;  // [2]
@@ -283,10 +292,11 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 4;
   uint64_t* o_free = pv_done + 2;
-  uint64_t* xch = o_free + 1;       // [quadrant][slot]: row-max / row-sum exchange, warps q and q + 4
-  uint64_t* drain = xch + 8;
+  uint64_t* drain = o_free + 1;
   uint64_t* o_staged = drain + 1;  // [Q slot]: the softmax warps have staged a tile-stored item's O
   uint64_t* drain2 = o_staged + 2;  // abort path of the PV issuer (drain: the S issuer)
+  uint64_t* stats_ready = drain2 + 1;  // the softmax warps have written an item's (m, l)
+  uint64_t* stats_free = stats_ready + 1;  // the epilogue warps have read them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
 
@@ -311,12 +321,13 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(p_full + 2 * i + 1, 4);
       mbar_init(pv_done + i, 1);
     }
-    mbar_init(o_free, 8);
-    for (int i = 0; i < 8; ++i) mbar_init(xch + i, 2);  // the two warps of a row quadrant
+    mbar_init(o_free, 4);  // one arrival per epilogue warp
     mbar_init(drain, 1);
     mbar_init(drain2, 1);
-    mbar_init(o_staged, 8);
-    mbar_init(o_staged + 1, 8);
+    mbar_init(o_staged, 4);
+    mbar_init(o_staged + 1, 4);
+    mbar_init(stats_ready, 8);
+    mbar_init(stats_free, 4);
     abort_set(abort_flag, 0);
     wait_limit_set(abort_flag, p.wait_ns);
     mbar_init_fence();
@@ -327,217 +338,337 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
-    // ================================================================ TMA producer
-    // Two streams over the same sequence of key tiles, polled without blocking: K (with each
-    // item's Q) and V.  Neither waits behind the other, so K tiles run ahead into their
-    // deeper ring while V waits for its PV to free a slot.  Every barrier tested here cannot
-    // complete its next phase before this thread issues another copy, so no phase is skipped.
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      TileCursor<CAUSAL, MODE> ck, cv;
-      ck.start(p, n_items);
-      cv.start(p, n_items);
-      uint32_t nq = 0;      // Q tiles issued (one per item, slot item % 2)
-      bool q_cur = false;   // the Q of ck's item has been issued
-      bool ok = true;
-      unsigned long long t_idle = 0;
-      while (!ck.done || !cv.done) {
-        bool progress = false;
-        const uint32_t qs = nq % SQ;
-        if (!ck.done && !q_cur && (nq < static_cast<uint32_t>(SQ) || mbar_test(q_empty + qs, ((nq / SQ) - 1) & 1))) {
-          const FwdItem& it = ck.it;
-          mbar_expect_tx(q_full + qs, L::kTileBytes);
-          for (int c = 0; c < kChunks; ++c) {
-            uint8_t* dst = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
-            if constexpr (VARLEN)
-              tma_load_4d(dst, &tmQ, q_full + qs, c * 64, it.h, 0, it.seq_start + it.qt * kBM);
-            else if constexpr (KV)
-              tma_load_3d(dst, &tmQ, q_full + qs, c * 64, it.qt * kBM, it.b * p.Hkv + it.h);
-            else
-              tma_load_3d(dst, &tmQ, q_full + qs, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
-          }
-          ++nq;
-          q_cur = true;
-          progress = true;
-        }
-        if (!ck.done && q_cur) {
-          const uint32_t st = ck.t % SK;
-          if (ck.t < static_cast<uint32_t>(SK) || mbar_test(k_empty + st, ((ck.t / SK) - 1) & 1)) {
+  if (warp >= 8 && warp < 12) {
+    regs_dec<L::kRegsIo>();
+    if (warp == 8) {
+      // ================================================================ TMA producer
+      // Two streams over the same sequence of key tiles, polled without blocking: K (with each
+      // item's Q) and V.  Neither waits behind the other, so K tiles run ahead into their
+      // deeper ring while V waits for its PV to free a slot.  Every barrier tested here cannot
+      // complete its next phase before this thread issues another copy, so no phase is skipped.
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        TileCursor<CAUSAL, MODE> ck, cv;
+        ck.start(p, n_items);
+        cv.start(p, n_items);
+        uint32_t nq = 0;      // Q tiles issued (one per item, slot item % 2)
+        bool q_cur = false;   // the Q of ck's item has been issued
+        bool ok = true;
+        unsigned long long t_idle = 0;
+        while (!ck.done || !cv.done) {
+          bool progress = false;
+          const uint32_t qs = nq % SQ;
+          if (!ck.done && !q_cur && (nq < static_cast<uint32_t>(SQ) || mbar_test(q_empty + qs, ((nq / SQ) - 1) & 1))) {
             const FwdItem& it = ck.it;
-            mbar_expect_tx(k_full + st, L::kTileBytes);
+            mbar_expect_tx(q_full + qs, L::kTileBytes);
             for (int c = 0; c < kChunks; ++c) {
-              uint8_t* dst = sK + st * L::kTileBytes + c * L::kChunkBytes;
+              uint8_t* dst = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
               if constexpr (VARLEN)
-                tma_load_4d(dst, &tmK, k_full + st, c * 64, it.h, 1, it.seq_start + ck.j * kBN);
+                tma_load_4d(dst, &tmQ, q_full + qs, c * 64, it.h, 0, it.seq_start + it.qt * kBM);
               else if constexpr (KV)
-                tma_load_3d(dst, &tmK, k_full + st, c * 64, (it.j0 + ck.j) * kBN, it.b * p.Hkv + it.h);
+                tma_load_3d(dst, &tmQ, q_full + qs, c * 64, it.qt * kBM, it.b * p.Hkv + it.h);
               else
-                tma_load_3d(dst, &tmK, k_full + st, c * 64, ck.j * kBN, it.b * p.Hkv + it.h / p.G);
+                tma_load_3d(dst, &tmQ, q_full + qs, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
             }
-            ck.advance(p, n_items);
-            if (ck.j == 0) q_cur = false;  // the next K belongs to a new item: its Q comes first
+            ++nq;
+            q_cur = true;
             progress = true;
           }
-        }
-        if (!cv.done) {
-          const uint32_t st = cv.t % SV;
-          if (cv.t < static_cast<uint32_t>(SV) || mbar_test(v_empty + st, ((cv.t / SV) - 1) & 1)) {
-            const FwdItem& it = cv.it;
-            mbar_expect_tx(v_full + st, L::kTileBytes);
-            for (int c = 0; c < kChunks; ++c) {
-              uint8_t* dst = sV + st * L::kTileBytes + c * L::kChunkBytes;
-              if constexpr (VARLEN)
-                tma_load_4d(dst, &tmV, v_full + st, c * 64, it.h, 2, it.seq_start + cv.j * kBN);
-              else if constexpr (KV)
-                tma_load_3d(dst, &tmV, v_full + st, c * 64, (it.j0 + cv.j) * kBN, it.b * p.Hkv + it.h);
-              else
-                tma_load_3d(dst, &tmV, v_full + st, c * 64, cv.j * kBN, it.b * p.Hkv + it.h / p.G);
+          if (!ck.done && q_cur) {
+            const uint32_t st = ck.t % SK;
+            if (ck.t < static_cast<uint32_t>(SK) || mbar_test(k_empty + st, ((ck.t / SK) - 1) & 1)) {
+              const FwdItem& it = ck.it;
+              mbar_expect_tx(k_full + st, L::kTileBytes);
+              for (int c = 0; c < kChunks; ++c) {
+                uint8_t* dst = sK + st * L::kTileBytes + c * L::kChunkBytes;
+                if constexpr (VARLEN)
+                  tma_load_4d(dst, &tmK, k_full + st, c * 64, it.h, 1, it.seq_start + ck.j * kBN);
+                else if constexpr (KV)
+                  tma_load_3d(dst, &tmK, k_full + st, c * 64, (it.j0 + ck.j) * kBN, it.b * p.Hkv + it.h);
+                else
+                  tma_load_3d(dst, &tmK, k_full + st, c * 64, ck.j * kBN, it.b * p.Hkv + it.h / p.G);
+              }
+              ck.advance(p, n_items);
+              if (ck.j == 0) q_cur = false;  // the next K belongs to a new item: its Q comes first
+              progress = true;
             }
-            cv.advance(p, n_items);
-            progress = true;
           }
-        }
-        if (progress) {
-          t_idle = 0;
-        } else {
-          const unsigned long long now = globaltimer();
-          if (t_idle == 0) t_idle = now;
-          if (abort_read(abort_flag)) { ok = false; break; }
-          if (now - t_idle > wait_limit(abort_flag)) {
-            raise_status(p.status, ATTN_ERR_TIMEOUT);
-            abort_set(abort_flag, 1);
-            ok = false;
-            break;
+          if (!cv.done) {
+            const uint32_t st = cv.t % SV;
+            if (cv.t < static_cast<uint32_t>(SV) || mbar_test(v_empty + st, ((cv.t / SV) - 1) & 1)) {
+              const FwdItem& it = cv.it;
+              mbar_expect_tx(v_full + st, L::kTileBytes);
+              for (int c = 0; c < kChunks; ++c) {
+                uint8_t* dst = sV + st * L::kTileBytes + c * L::kChunkBytes;
+                if constexpr (VARLEN)
+                  tma_load_4d(dst, &tmV, v_full + st, c * 64, it.h, 2, it.seq_start + cv.j * kBN);
+                else if constexpr (KV)
+                  tma_load_3d(dst, &tmV, v_full + st, c * 64, (it.j0 + cv.j) * kBN, it.b * p.Hkv + it.h);
+                else
+                  tma_load_3d(dst, &tmV, v_full + st, c * 64, cv.j * kBN, it.b * p.Hkv + it.h / p.G);
+              }
+              cv.advance(p, n_items);
+              progress = true;
+            }
           }
-        }
-      }
-      if (!ok || abort_read(abort_flag)) {
-        // let the copies already issued land before the CTA's shared memory goes away
-        for (uint32_t n = nq > static_cast<uint32_t>(SQ) ? nq - SQ : 0; n < nq; ++n)
-          mbar_drain(q_full + n % SQ, (n / SQ) & 1);
-        for (uint32_t j = ck.t > static_cast<uint32_t>(SK) ? ck.t - SK : 0; j < ck.t; ++j)
-          mbar_drain(k_full + j % SK, (j / SK) & 1);
-        for (uint32_t j = cv.t > static_cast<uint32_t>(SV) ? cv.t - SV : 0; j < cv.t; ++j)
-          mbar_drain(v_full + j % SV, (j / SV) & 1);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 9 || warp == 11) {
-    // ================================================================ MMA issuers
-    // Two threads on two sub-partitions: warp 9 issues the S stream, warp 11 the PV stream (one
-    // thread issues a tcgen05.mma about every 64 cycles at best, and slower when busy warps share
-    // its sub-partition: two issuers keep the tensor core fed).  The streams touch disjoint TMEM
-    // (S buffers; P buffers and O) and are ordered only through the softmax's barriers.
-    if (lane == 0) {
-      constexpr bool kB = Elem<T>::kBf16;
-      constexpr uint32_t idS = idesc_f16(kB, false, false, 128, kBN);
-      constexpr uint32_t idO = idesc_f16(kB, false, true, 128, DP);
-      const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dV = smem_desc_sw128(smem_u32(sV), L::kChunkBytes, 1024);
-      const bool s_side = warp == 9;
-      bool ok = true;
-      uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
-      uint32_t ic = 0;
-      for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
-        const int idx = cta_item<MODE>(k);
-        if (idx >= n_items) continue;
-        const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
-        if (!it.valid) continue;
-        const int n = it.n_kv;
-        const uint32_t qs = ic % SQ;
-        if (s_side) {
-          if (!mbar_wait(q_full + qs, (ic / SQ) & 1, abort_flag, p.status)) { ok = false; break; }
-          for (int j = 0; j < n; ++j) {
-            const uint32_t t = kv + j;
-            // S buffer t % 2 holds P(t-2) until PV(t-2) has read it
-            if (!mbar_wait(k_full + t % SK, (t / SK) & 1, abort_flag, p.status) ||
-                (t >= 2 && !mbar_wait(pv_done + (t & 1), ((t - 2) >> 1) & 1, abort_flag, p.status))) {
+          if (progress) {
+            t_idle = 0;
+          } else {
+            const unsigned long long now = globaltimer();
+            if (t_idle == 0) t_idle = now;
+            if (abort_read(abort_flag)) { ok = false; break; }
+            if (now - t_idle > wait_limit(abort_flag)) {
+              raise_status(p.status, ATTN_ERR_TIMEOUT);
+              abort_set(abort_flag, 1);
               ok = false;
               break;
             }
-            tc_fence_after();
-            const uint64_t qx = dQ + ((qs * L::kTileBytes) >> 4);
-            const uint64_t kx = dK + (((t % SK) * L::kTileBytes) >> 4);
-            const uint32_t d = tmem + (t & 1) * 128;
-#pragma unroll
-            for (int ks = 0; ks < DP / 16; ++ks) {
-              const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-              mma_ss(d, qx + off, kx + off, idS, ks > 0 ? 1u : 0u);
-            }
-            mma_commit(s_full + (t & 1));
-            mma_commit(k_empty + t % SK);
-            if (j == n - 1 && !tile_item(it)) mma_commit(q_empty + qs);
           }
-        } else {
-          for (int j = 0; j < n; ++j) {
-            const uint32_t t = kv + j;
-            const uint32_t b = t & 1;
-            if (!mbar_wait(v_full + t % SV, (t / SV) & 1, abort_flag, p.status) ||
-                (j == 0 && ic > 0 && !mbar_wait(o_free, (ic - 1) & 1, abort_flag, p.status))) {
-              ok = false;
-              break;
-            }
-            const uint64_t vx = dV + (((t % SV) * L::kTileBytes) >> 4);
-            const uint32_t acc0 = j == 0 ? 0u : 1u;
-            // PV_g(t): O_g (+)= P_g(t) V[64g, 64g + 64), P_g over the first 32 columns of group
-            // g's half of S buffer b (keys 2c, 2c+1 in column c)
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-              if (!mbar_wait(p_full + 2 * b + g, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        }
+        if (!ok || abort_read(abort_flag)) {
+          // let the copies already issued land before the CTA's shared memory goes away
+          for (uint32_t n = nq > static_cast<uint32_t>(SQ) ? nq - SQ : 0; n < nq; ++n)
+            mbar_drain(q_full + n % SQ, (n / SQ) & 1);
+          for (uint32_t j = ck.t > static_cast<uint32_t>(SK) ? ck.t - SK : 0; j < ck.t; ++j)
+            mbar_drain(k_full + j % SK, (j / SK) & 1);
+          for (uint32_t j = cv.t > static_cast<uint32_t>(SV) ? cv.t - SV : 0; j < cv.t; ++j)
+            mbar_drain(v_full + j % SV, (j / SV) & 1);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 9 || warp == 11) {
+      // ================================================================ MMA issuers
+      // Two threads on two sub-partitions: warp 9 issues the S stream, warp 11 the PV stream (one
+      // thread issues a tcgen05.mma about every 64 cycles at best, and slower when busy warps share
+      // its sub-partition: two issuers keep the tensor core fed).  The streams touch disjoint TMEM
+      // (S buffers; P buffers and O) and are ordered only through the softmax's barriers.
+      if (lane == 0) {
+        constexpr bool kB = Elem<T>::kBf16;
+        constexpr uint32_t idS = idesc_f16(kB, false, false, 128, kBN);
+        constexpr uint32_t idO = idesc_f16(kB, false, true, 128, DP);
+        const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t dV = smem_desc_sw128(smem_u32(sV), L::kChunkBytes, 1024);
+        const bool s_side = warp == 9;
+        bool ok = true;
+        uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
+        uint32_t ic = 0;
+        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+          const int idx = cta_item<MODE>(k);
+          if (idx >= n_items) continue;
+          const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
+          if (!it.valid) continue;
+          const int n = it.n_kv;
+          const uint32_t qs = ic % SQ;
+          if (s_side) {
+            if (!mbar_wait(q_full + qs, (ic / SQ) & 1, abort_flag, p.status)) { ok = false; break; }
+            for (int j = 0; j < n; ++j) {
+              const uint32_t t = kv + j;
+              // S buffer t % 2 holds P(t-2) until PV(t-2) has read it
+              if (!mbar_wait(k_full + t % SK, (t / SK) & 1, abort_flag, p.status) ||
+                  (t >= 2 && !mbar_wait(pv_done + (t & 1), ((t - 2) >> 1) & 1, abort_flag, p.status))) {
+                ok = false;
+                break;
+              }
               tc_fence_after();
-              const uint32_t pa = tmem + b * 128 + g * 64;
+              const uint64_t qx = dQ + ((qs * L::kTileBytes) >> 4);
+              const uint64_t kx = dK + (((t % SK) * L::kTileBytes) >> 4);
+              const uint32_t d = tmem + (t & 1) * 128;
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                mma_ts(tmem + L::kColO + g * DP, pa + ks * 8, vx + (((4 * g + ks) * 2048) >> 4), idO,
-                       ks > 0 ? 1u : acc0);
+              for (int ks = 0; ks < DP / 16; ++ks) {
+                const uint32_t off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+                mma_ss(d, qx + off, kx + off, idS, ks > 0 ? 1u : 0u);
+              }
+              mma_commit(s_full + (t & 1));
+              mma_commit(k_empty + t % SK);
+              if (j == n - 1 && !tile_item(it)) mma_commit(q_empty + qs);
             }
-            if (!ok) break;
-            mma_commit(pv_done + b);
-            mma_commit(v_empty + t % SV);
+          } else {
+            for (int j = 0; j < n; ++j) {
+              const uint32_t t = kv + j;
+              const uint32_t b = t & 1;
+              if (!mbar_wait(v_full + t % SV, (t / SV) & 1, abort_flag, p.status) ||
+                  (j == 0 && ic > 0 && !mbar_wait(o_free, (ic - 1) & 1, abort_flag, p.status))) {
+                ok = false;
+                break;
+              }
+              const uint64_t vx = dV + (((t % SV) * L::kTileBytes) >> 4);
+              const uint32_t acc0 = j == 0 ? 0u : 1u;
+              // PV_g(t): O_g (+)= P_g(t) V[64g, 64g + 64), P_g over the first 32 columns of group
+              // g's half of S buffer b (keys 2c, 2c+1 in column c)
+#pragma unroll
+              for (int g = 0; g < 2; ++g) {
+                if (!mbar_wait(p_full + 2 * b + g, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t pa = tmem + b * 128 + g * 64;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                  mma_ts(tmem + L::kColO + g * DP, pa + ks * 8, vx + (((4 * g + ks) * 2048) >> 4), idO,
+                         ks > 0 ? 1u : acc0);
+              }
+              if (!ok) break;
+              mma_commit(pv_done + b);
+              mma_commit(v_empty + t % SV);
+            }
+          }
+          kv += n;
+          ++ic;
+        }
+        if (!ok) {
+          uint64_t* dr = s_side ? drain : drain2;
+          mma_commit(dr);  // every MMA this thread issued completes before this arrives
+          mbar_drain(dr, 0);
+        }
+      }
+      __syncwarp();
+    } else {
+      // ================================================================ output tile stores
+      if (lane == 0 && tile_out) {
+        tma_prefetch_desc(&tmO);
+        uint32_t ic = 0, nt[2] = {0, 0};  // items; per Q slot, items stored by tiles (o_staged phases)
+        for (int k = 0; k * static_cast<int>(gridDim.x) < n_items; ++k) {
+          const int idx = cta_item<MODE>(k);
+          if (idx >= n_items) continue;
+          const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
+          if (!it.valid) continue;
+          const uint32_t qs = ic++ % SQ;
+          if (!tile_item(it)) continue;
+          if (!mbar_wait(o_staged + qs, nt[qs]++ & 1, abort_flag, p.status)) break;
+          for (int c = 0; c < kChunks; ++c) {
+            const uint8_t* src = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
+            if constexpr (VARLEN)  // map {d, T, H} over the [T, H, d] output
+              tma_store_3d(&tmO, src, c * 64, it.seq_start + it.qt * kBM, it.h);
+            else
+              tma_store_3d(&tmO, src, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
+          }
+          bulk_commit();
+          bulk_wait_read<0>();
+          mbar_arrive(q_empty + qs);  // the slot may take the Q of the item after next
+        }
+        bulk_wait_all();  // the stores are complete before the CTA ends
+      }
+      __syncwarp();
+  }
+  } else if (warp >= 12) {
+    regs_dec<L::kRegsEpi>();
+    // ================================================================ epilogue warpgroup
+    // Per item, thread t (row t): both groups' (max, sum) from the softmax warps, then, once the
+    // item's last PV has completed, O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l over the whole
+    // row, released from TMEM as soon as it is loaded (o_free), and LSE = m + ln l.  16-bit
+    // tiles are staged in the item's Q slot for the store warp; otherwise rows are stored here.
+    const int row = threadIdx.x - 384;  // TMEM lane
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    uint32_t kv = 0, ic = 0;
+    bool ok = true;
+    for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
+      const int idx = cta_item<MODE>(k);
+      if (idx >= n_items) continue;
+      const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
+      if (!it.valid) continue;
+      const int q_row = it.qt * kBM + row;
+      kv += it.n_kv;
+      if (!mbar_wait_warp(stats_ready, ic & 1, abort_flag, p.status)) { ok = false; break; }
+      const float2 s0 = sStats[row], s1 = sStats[128 + row];
+      mbar_arrive_warp(stats_free);
+      const float mr = fmaxf(s0.x, s1.x);
+      const float a0 = (s0.x == -INFINITY) ? 0.f : ex2_approx(s0.x - mr);
+      const float a1 = (s1.x == -INFINITY) ? 0.f : ex2_approx(s1.x - mr);
+      const float l_all = s0.y * a0 + s1.y * a1;
+      const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
+      const float c0 = a0 * inv_l, c1 = a1 * inv_l;  // weights of O_0 and O_1
+      const uint32_t t_last = kv - 1;
+      if (!mbar_wait_warp(pv_done + (t_last & 1), (t_last >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const bool valid = q_row < (KV ? p.R : it.seq_len);
+      size_t row_off;
+      // a KV cache range writes its partial output in fp32 to its slice of the split buffer
+      const size_t kv_row = KV ? (static_cast<size_t>(it.split) * p.B * p.Hkv + static_cast<size_t>(it.b) * p.Hkv + it.h) * p.R + q_row : 0;
+      if constexpr (VARLEN)
+        row_off = (static_cast<size_t>(it.seq_start + q_row) * p.Hq + it.h) * p.d;
+      else if constexpr (KV)
+        row_off = kv_row * p.d;
+      else
+        row_off = ((static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row) * p.d;
+      const bool o_f32 = KV || p.out_f32;
+      void* const o_base = KV ? static_cast<void*>(p.o_part) : p.o;
+      const bool tile = tile_item(it);
+      uint8_t* srow = sQ + (ic % SQ) * L::kTileBytes + row * 128;
+#pragma unroll 1
+      for (int c = 0; c < DP / 32; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tl + L::kColO + c * 32, r0);
+        tmem_ld32(tl + L::kColO + DP + c * 32, r1);
+        tmem_ld_wait();
+        tmem_reg_fence(r0);
+        tmem_reg_fence(r1);
+        if (c == DP / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive_warp(o_free);  // both accumulators are in registers: the next item may overwrite them
+        }
+        float o[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r0[i]) * c0 + __uint_as_float(r1[i]) * c1;
+        if (tile) {
+          // the item's Q slot, in the 128-byte swizzled layout of the output map's {64, 128} boxes:
+          // column col lands in box col / 64, 16-byte granule (col % 64) / 8; rows and columns past
+          // the tensor are clipped by the store
+          uint8_t* brow = srow + ((c * 32) / 64) * L::kChunkBytes;
+          const int gran0 = ((c * 32) % 64) / 8;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 v;
+            v.x = Elem<T>::pack(o[8 * i + 0], o[8 * i + 1]);
+            v.y = Elem<T>::pack(o[8 * i + 2], o[8 * i + 3]);
+            v.z = Elem<T>::pack(o[8 * i + 4], o[8 * i + 5]);
+            v.w = Elem<T>::pack(o[8 * i + 6], o[8 * i + 7]);
+            const int gran = gran0 + i;
+            *reinterpret_cast<uint4*>(brow + ((gran ^ (row & 7)) << 4)) = v;
+          }
+        } else {
+          const int col0 = c * 32;
+          if (valid && col0 < p.d) {
+            const int ncol = min(32, p.d - col0);  // 16 or 32 (d is a multiple of 16)
+            if (o_f32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o_base) + row_off + col0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (i * 4 < ncol) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(o_base) + row_off + col0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (i * 8 < ncol) {
+                  uint4 v;
+                  v.x = Elem<T>::pack(o[8 * i + 0], o[8 * i + 1]);
+                  v.y = Elem<T>::pack(o[8 * i + 2], o[8 * i + 3]);
+                  v.z = Elem<T>::pack(o[8 * i + 4], o[8 * i + 5]);
+                  v.w = Elem<T>::pack(o[8 * i + 6], o[8 * i + 7]);
+                  dst[i] = v;
+                }
+              }
+            }
           }
         }
-        kv += n;
-        ++ic;
       }
-      if (!ok) {
-        uint64_t* dr = s_side ? drain : drain2;
-        mma_commit(dr);  // every MMA this thread issued completes before this arrives
-        mbar_drain(dr, 0);
+      if (tile) {
+        fence_async_smem();
+        mbar_arrive_warp(o_staged + ic % SQ);
       }
+      if (valid && (KV || p.lse)) {
+        const float lse = (mr + __log2f(l_all)) * 0.69314718055994531f;
+        if constexpr (KV)
+          p.lse_part[kv_row] = lse;
+        else if constexpr (VARLEN)
+          p.lse[static_cast<size_t>(it.h) * p.total_tokens + it.seq_start + q_row] = lse;
+        else
+          p.lse[(static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row] = lse;
+      }
+      ++ic;
     }
-    __syncwarp();
-  } else if (warp == 10) {
-    // ================================================================ output tile stores
-    if (lane == 0 && tile_out) {
-      tma_prefetch_desc(&tmO);
-      uint32_t ic = 0, nt[2] = {0, 0};  // items; per Q slot, items stored by tiles (o_staged phases)
-      for (int k = 0; k * static_cast<int>(gridDim.x) < n_items; ++k) {
-        const int idx = cta_item<MODE>(k);
-        if (idx >= n_items) continue;
-        const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
-        if (!it.valid) continue;
-        const uint32_t qs = ic++ % SQ;
-        if (!tile_item(it)) continue;
-        if (!mbar_wait(o_staged + qs, nt[qs]++ & 1, abort_flag, p.status)) break;
-        for (int c = 0; c < kChunks; ++c) {
-          const uint8_t* src = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
-          if constexpr (VARLEN)  // map {d, T, H} over the [T, H, d] output
-            tma_store_3d(&tmO, src, c * 64, it.seq_start + it.qt * kBM, it.h);
-          else
-            tma_store_3d(&tmO, src, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
-        }
-        bulk_commit();
-        bulk_wait_read<0>();
-        mbar_arrive(q_empty + qs);  // the slot may take the Q of the item after next
-      }
-      bulk_wait_all();  // the stores are complete before the CTA ends
-    }
-    __syncwarp();
   } else {
+    regs_inc<L::kRegsSmx>();
     // ================================================================ softmax groups
     const int grp = warp >> 2;                // 0: key columns 0-63, 1: key columns 64-127
     const int row = threadIdx.x & 127;        // TMEM lane
@@ -545,19 +676,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tOg = tl + L::kColO + grp * DP;  // this group's accumulator O_g
     const float sl2 = p.scale_log2;
     uint32_t kv = 0, ic = 0;
-    uint32_t xc = 0;  // exchanges done (slot xc % 2, phase (xc / 2) % 2)
     bool ok = true;
-    // Writes this thread's value to the exchange slot and returns the other group's value.
-    auto exchange = [&](float v, float& other) -> bool {
-      float* xb = sX + (xc & 1) * 256;
-      xb[grp * 128 + row] = v;
-      uint64_t* bar = xch + (warp & 3) * 2 + (xc & 1);
-      mbar_arrive_warp(bar);
-      if (!mbar_wait_warp(bar, (xc >> 1) & 1, abort_flag, p.status)) return false;
-      other = xb[(grp ^ 1) * 128 + row];
-      ++xc;
-      return true;
-    };
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
       const int idx = cta_item<MODE>(k);
       if (idx >= n_items) continue;
@@ -682,106 +801,11 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       kv += it.n_kv;
-      // ---- epilogue: the row's max and sum from both groups; O = (O_0 a_0 + O_1 a_1) / l
-      float mo, lo;
-      if (!exchange(m, mo) || !exchange(l, lo)) { ok = false; break; }
-      const float mr = fmaxf(m, mo);
-      const float a_self = (m == -INFINITY) ? 0.f : ex2_approx(m - mr);
-      const float a_other = (mo == -INFINITY) ? 0.f : ex2_approx(mo - mr);
-      const float l_all = l * a_self + lo * a_other;
-      const uint32_t tl_last = kv - 1;
-      if (!mbar_wait_warp(pv_done + (tl_last & 1), (tl_last >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-      tc_fence_after();
-      const bool valid = q_row < (KV ? p.R : it.seq_len);
-      const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
-      // weights of O_0 and O_1 in this row's output
-      const float c0 = (grp == 0 ? a_self : a_other) * inv_l, c1 = (grp == 0 ? a_other : a_self) * inv_l;
-      size_t row_off;
-      // a KV cache range writes its partial output in fp32 to its slice of the split buffer
-      const size_t kv_row = KV ? (static_cast<size_t>(it.split) * p.B * p.Hkv + static_cast<size_t>(it.b) * p.Hkv + it.h) * p.R + q_row : 0;
-      if constexpr (VARLEN)
-        row_off = (static_cast<size_t>(it.seq_start + q_row) * p.Hq + it.h) * p.d;
-      else if constexpr (KV)
-        row_off = kv_row * p.d;
-      else
-        row_off = ((static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row) * p.d;
-      const bool o_f32 = KV || p.out_f32;
-      void* const o_base = KV ? static_cast<void*>(p.o_part) : p.o;
-      const bool tile = tile_item(it);
-      // this thread's DP / 2 output columns, from column grp * DP / 2, 32 at a time: both
-      // accumulators loaded, combined in registers
-      constexpr int kHalf = DP / 2;
-      const uint32_t tO0 = tl + L::kColO + grp * kHalf, tO1 = tO0 + DP;
-      uint8_t* srow = sQ + (ic % SQ) * L::kTileBytes + ((grp * kHalf) / 64) * L::kChunkBytes + row * 128;
-      const int gran0 = ((grp * kHalf) % 64) / 8;
-#pragma unroll
-      for (int c = 0; c < DP / 64; ++c) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tO0 + c * 32, r0);
-        tmem_ld32(tO1 + c * 32, r1);
-        tmem_ld_wait();
-        tmem_reg_fence(r0);
-        tmem_reg_fence(r1);
-        if (c == DP / 64 - 1) {
-          tc_fence_before();
-          mbar_arrive_warp(o_free);  // both accumulators are in registers: the next item may overwrite them
-        }
-        float o[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r0[i]) * c0 + __uint_as_float(r1[i]) * c1;
-        if (tile) {
-          // into the item's Q slot, in the 128-byte swizzled layout of the output map's {64, 128}
-          // boxes: column col lands in box col / 64, 16-byte granule (col % 64) / 8; rows and
-          // columns past the tensor are clipped by the store
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 v;
-            v.x = Elem<T>::pack(o[8 * i + 0], o[8 * i + 1]);
-            v.y = Elem<T>::pack(o[8 * i + 2], o[8 * i + 3]);
-            v.z = Elem<T>::pack(o[8 * i + 4], o[8 * i + 5]);
-            v.w = Elem<T>::pack(o[8 * i + 6], o[8 * i + 7]);
-            const int gran = gran0 + c * 4 + i;
-            *reinterpret_cast<uint4*>(srow + ((gran ^ (row & 7)) << 4)) = v;
-          }
-        } else {
-          const int col0 = grp * kHalf + c * 32;
-          if (valid && col0 < p.d) {
-            const int ncol = min(32, p.d - col0);  // 16 or 32 (d is a multiple of 16)
-            if (o_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o_base) + row_off + col0);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                if (i * 4 < ncol) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(o_base) + row_off + col0);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                if (i * 8 < ncol) {
-                  uint4 v;
-                  v.x = Elem<T>::pack(o[8 * i + 0], o[8 * i + 1]);
-                  v.y = Elem<T>::pack(o[8 * i + 2], o[8 * i + 3]);
-                  v.z = Elem<T>::pack(o[8 * i + 4], o[8 * i + 5]);
-                  v.w = Elem<T>::pack(o[8 * i + 6], o[8 * i + 7]);
-                  dst[i] = v;
-                }
-              }
-            }
-          }
-        }
-      }
-      if (tile) {
-        fence_async_smem();
-        mbar_arrive_warp(o_staged + ic % SQ);
-      }
-      if (grp == 0 && valid && (KV || p.lse)) {
-        const float lse = (mr + __log2f(l_all)) * 0.69314718055994531f;
-        if constexpr (KV)
-          p.lse_part[kv_row] = lse;
-        else if constexpr (VARLEN)
-          p.lse[static_cast<size_t>(it.h) * p.total_tokens + it.seq_start + q_row] = lse;
-        else
-          p.lse[(static_cast<size_t>(it.b) * p.Hq + it.h) * p.N + q_row] = lse;
-      }
+      // ---- hand the item's (max, sum) to the epilogue warpgroup, then straight on to the next
+      // item: the epilogue combines O_0 and O_1 while this item's successor is computed
+      if (ic >= 1 && !mbar_wait_warp(stats_free, (ic - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      sStats[grp * 128 + row] = make_float2(m, l);
+      mbar_arrive_warp(stats_ready);
       ++ic;
     }
   }
@@ -811,6 +835,11 @@ cudaError_t launch_fwd_tc_t(const FwdMaps& maps, const FwdParams& p, cudaStream_
   auto kern = fwd_tc_kernel<T, DP, CAUSAL, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
+  // The in-kernel register split assumes the launch allocation; never launch otherwise.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != static_cast<int>(L::kLaunchRegs)) return cudaErrorInvalidConfiguration;
   const long heads = MODE == kModeVarlen ? static_cast<long>(p.Hq) * p.nseq
                      : MODE == kModeKv   ? static_cast<long>(p.B) * p.Hkv * p.n_splits
                                          : static_cast<long>(p.B) * p.Hq;
