@@ -24,12 +24,13 @@
 //              hands its (max, sum) to the epilogue warps and goes on to the next item.
 //   warp 8     TMA producer (lane 0) and TMEM allocator (whole warp).
 //   warp 9     MMA issuer of the S(j) stream (lane 0).
-//   warp 10    output tile stores (lane 0): writes each staged O tile with TMA and frees the
-//              Q slot.
-//   warp 11    MMA issuer of the PV(j) stream (lane 0).
+//   warps 11, 10  MMA issuers of the PV_0(j) and PV_1(j) streams (lane 0): one thread issues an
+//              MMA only every ~110 cycles while busy softmax warps share its sub-partition, so
+//              the two groups' PVs go in from two sub-partitions.
 //   warps 12-15 epilogue: per item, once its last PV has completed, combine O_0 and O_1 with
-//              the two groups' (max, sum) into O / l and LSE, staged for the tile stores or
-//              stored per row, while the softmax warps already work on the next item.
+//              the two groups' (max, sum) into O / l and LSE, staged in the item's Q slot and
+//              written with TMA tile stores by warp 12 (which then frees the slot), or stored
+//              per row, while the softmax warps already work on the next item.
 // Registers: launched at 128 per thread, then split per warpgroup with setmaxnreg (softmax
 // 168, I/O 56, epilogue 120).
 // TMEM: S double buffer at columns [0,128) and [128,256), P(j) of group g over columns
@@ -96,9 +97,9 @@ struct FwdLayout {
   // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
   // p_full[2 buffers][2 groups], pv_done[2], o_free, drain,
   // o_staged[2] (per Q slot, so it cannot run two phases ahead of the store warp: a slot takes
-  // a new Q only after the store warp has written out the tile staged in it), drain2,
+  // a new Q only after the tile staged in it has been written out), drain2, drain3,
   // stats_ready, stats_free
-  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 4 + 2 + 1 + 1 + 2 + 1 + 2;
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 4 + 2 + 1 + 1 + 2 + 2 + 2;
   // tmem base (u32), abort flag (int), wait limit (u64, ns)
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kBytes = kOffMisc + 16;
@@ -287,15 +288,17 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* v_full = k_empty + SK;
   uint64_t* v_empty = v_full + SV;
   // Per buffer b: s_full (S(j) ready), p_full[b * 2 + g] (group g has written P(j)), pv_done
-  // (PV(j) of both groups done), for the tiles j with j % 2 == b; phase k is tile 2k + b.
+  // (PV(j) of both groups done: one commit from each PV issuer), for the tiles j with
+  // j % 2 == b; phase k is tile 2k + b.
   uint64_t* s_full = v_empty + SV;
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 4;
   uint64_t* o_free = pv_done + 2;
   uint64_t* drain = o_free + 1;
   uint64_t* o_staged = drain + 1;  // [Q slot]: the softmax warps have staged a tile-stored item's O
-  uint64_t* drain2 = o_staged + 2;  // abort path of the PV issuer (drain: the S issuer)
-  uint64_t* stats_ready = drain2 + 1;  // the softmax warps have written an item's (m, l)
+  uint64_t* drain2 = o_staged + 2;  // abort paths of the PV issuers (drain: the S issuer)
+  uint64_t* drain3 = drain2 + 1;
+  uint64_t* stats_ready = drain3 + 1;  // the softmax warps have written an item's (m, l)
   uint64_t* stats_free = stats_ready + 1;  // the epilogue warps have read them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   const uint32_t abort_flag = smem_u32(smem + L::kOffMisc + 4);  // CTA abort flag (shared)
@@ -313,17 +316,18 @@ __global__ void __launch_bounds__(512, 1)
     }
     for (int i = 0; i < SV; ++i) {
       mbar_init(v_full + i, 1);
-      mbar_init(v_empty + i, 1);
+      mbar_init(v_empty + i, 2);  // one commit from each PV issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
       mbar_init(p_full + 2 * i, 4);  // one arrival per softmax warp of the group
       mbar_init(p_full + 2 * i + 1, 4);
-      mbar_init(pv_done + i, 1);
+      mbar_init(pv_done + i, 2);
     }
     mbar_init(o_free, 4);  // one arrival per epilogue warp
     mbar_init(drain, 1);
     mbar_init(drain2, 1);
+    mbar_init(drain3, 1);
     mbar_init(o_staged, 4);
     mbar_init(o_staged + 1, 4);
     mbar_init(stats_ready, 8);
@@ -438,12 +442,13 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
       __syncwarp();
-    } else if (warp == 9 || warp == 11) {
+    } else {
       // ================================================================ MMA issuers
-      // Two threads on two sub-partitions: warp 9 issues the S stream, warp 11 the PV stream (one
-      // thread issues a tcgen05.mma about every 64 cycles at best, and slower when busy warps share
-      // its sub-partition: two issuers keep the tensor core fed).  The streams touch disjoint TMEM
-      // (S buffers; P buffers and O) and are ordered only through the softmax's barriers.
+      // Three threads on three sub-partitions: warp 9 issues the S stream, warps 11 and 10 the PV
+      // streams of groups 0 and 1 (one thread issues a tcgen05.mma about every 64 cycles at best,
+      // and at about half that rate when busy warps share its sub-partition).  The streams touch
+      // disjoint TMEM (S buffers; P_0 / O_0; P_1 / O_1) and are ordered only through the
+      // softmax's barriers.
       if (lane == 0) {
         constexpr bool kB = Elem<T>::kBf16;
         constexpr uint32_t idS = idesc_f16(kB, false, false, 128, kBN);
@@ -452,6 +457,7 @@ __global__ void __launch_bounds__(512, 1)
         const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
         const uint64_t dV = smem_desc_sw128(smem_u32(sV), L::kChunkBytes, 1024);
         const bool s_side = warp == 9;
+        const int g = warp == 11 ? 0 : 1;  // the PV issuer's group
         bool ok = true;
         uint32_t kv = 0;  // global key-tile counter (ring position and S/P/PV phases)
         uint32_t ic = 0;
@@ -498,17 +504,13 @@ __global__ void __launch_bounds__(512, 1)
               const uint32_t acc0 = j == 0 ? 0u : 1u;
               // PV_g(t): O_g (+)= P_g(t) V[64g, 64g + 64), P_g over the first 32 columns of group
               // g's half of S buffer b (keys 2c, 2c+1 in column c)
+              if (!mbar_wait(p_full + 2 * b + g, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t pa = tmem + b * 128 + g * 64;
+              const uint64_t vg = vx + ((g * 4 * 2048) >> 4);
 #pragma unroll
-              for (int g = 0; g < 2; ++g) {
-                if (!mbar_wait(p_full + 2 * b + g, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t pa = tmem + b * 128 + g * 64;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                  mma_ts(tmem + L::kColO + g * DP, pa + ks * 8, vx + (((4 * g + ks) * 2048) >> 4), idO,
-                         ks > 0 ? 1u : acc0);
-              }
-              if (!ok) break;
+              for (int ks = 0; ks < 4; ++ks)
+                mma_ts(tmem + L::kColO + g * DP, pa + ks * 8, vg + ((ks * 2048) >> 4), idO, ks > 0 ? 1u : acc0);
               mma_commit(pv_done + b);
               mma_commit(v_empty + t % SV);
             }
@@ -517,37 +519,10 @@ __global__ void __launch_bounds__(512, 1)
           ++ic;
         }
         if (!ok) {
-          uint64_t* dr = s_side ? drain : drain2;
+          uint64_t* dr = s_side ? drain : (g == 0 ? drain2 : drain3);
           mma_commit(dr);  // every MMA this thread issued completes before this arrives
           mbar_drain(dr, 0);
         }
-      }
-      __syncwarp();
-    } else {
-      // ================================================================ output tile stores
-      if (lane == 0 && tile_out) {
-        tma_prefetch_desc(&tmO);
-        uint32_t ic = 0, nt[2] = {0, 0};  // items; per Q slot, items stored by tiles (o_staged phases)
-        for (int k = 0; k * static_cast<int>(gridDim.x) < n_items; ++k) {
-          const int idx = cta_item<MODE>(k);
-          if (idx >= n_items) continue;
-          const FwdItem it = fwd_item<CAUSAL, MODE>(p, idx);
-          if (!it.valid) continue;
-          const uint32_t qs = ic++ % SQ;
-          if (!tile_item(it)) continue;
-          if (!mbar_wait(o_staged + qs, nt[qs]++ & 1, abort_flag, p.status)) break;
-          for (int c = 0; c < kChunks; ++c) {
-            const uint8_t* src = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
-            if constexpr (VARLEN)  // map {d, T, H} over the [T, H, d] output
-              tma_store_3d(&tmO, src, c * 64, it.seq_start + it.qt * kBM, it.h);
-            else
-              tma_store_3d(&tmO, src, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
-          }
-          bulk_commit();
-          bulk_wait_read<0>();
-          mbar_arrive(q_empty + qs);  // the slot may take the Q of the item after next
-        }
-        bulk_wait_all();  // the stores are complete before the CTA ends
       }
       __syncwarp();
   }
@@ -560,7 +535,9 @@ __global__ void __launch_bounds__(512, 1)
     // tiles are staged in the item's Q slot for the store warp; otherwise rows are stored here.
     const int row = threadIdx.x - 384;  // TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    uint32_t kv = 0, ic = 0;
+    const bool storer = row == 0 && tile_out;  // issues the tile stores of staged items
+    if (storer) tma_prefetch_desc(&tmO);
+    uint32_t kv = 0, ic = 0, nt[2] = {0, 0};  // nt: per Q slot, items stored by tiles (o_staged phases)
     bool ok = true;
     for (int k = 0; ok && k * static_cast<int>(gridDim.x) < n_items; ++k) {
       const int idx = cta_item<MODE>(k);
@@ -655,6 +632,26 @@ __global__ void __launch_bounds__(512, 1)
       if (tile) {
         fence_async_smem();
         mbar_arrive_warp(o_staged + ic % SQ);
+        // once all four warps have staged their rows: write the tile out, then free the Q slot
+        // for the Q of the item after next
+        const uint32_t qs = ic % SQ;
+        if (storer) {
+          if (!mbar_wait(o_staged + qs, nt[qs]++ & 1, abort_flag, p.status)) {
+            ok = false;
+          } else {
+            for (int c = 0; c < kChunks; ++c) {
+              const uint8_t* src = sQ + qs * L::kTileBytes + c * L::kChunkBytes;
+              if constexpr (VARLEN)  // map {d, T, H} over the [T, H, d] output
+                tma_store_3d(&tmO, src, c * 64, it.seq_start + it.qt * kBM, it.h);
+              else
+                tma_store_3d(&tmO, src, c * 64, it.qt * kBM, it.b * p.Hq + it.h);
+            }
+            bulk_commit();
+            bulk_wait_read<0>();
+            mbar_arrive(q_empty + qs);
+          }
+        }
+        if (warp == 12) ok = __all_sync(0xffffffffu, ok);  // the warp leaves the loop together
       }
       if (valid && (KV || p.lse)) {
         const float lse = (mr + __log2f(l_all)) * 0.69314718055994531f;
@@ -667,6 +664,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       ++ic;
     }
+    if (storer) bulk_wait_all();  // the tile stores are complete before the CTA ends
   } else {
     regs_inc<L::kRegsSmx>();
     // ================================================================ softmax groups
