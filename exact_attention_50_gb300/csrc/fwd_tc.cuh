@@ -95,11 +95,11 @@ struct FwdLayout {
   static constexpr int kOffX = kOffV + kStagesV * kTileBytes;  // item end (m, l): [2 groups][128 rows]
   static constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
   // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
-  // p_full[2 buffers][2 groups], pv_done[2], o_free, drain,
+  // p_full[2 buffers][2 groups][2 halves], pv_done[2], o_free, drain,
   // o_staged[2] (per Q slot, so it cannot run two phases ahead of the store warp: a slot takes
   // a new Q only after the tile staged in it has been written out), drain2, drain3,
   // stats_ready, stats_free
-  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 4 + 2 + 1 + 1 + 2 + 2 + 2;
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 8 + 2 + 1 + 1 + 2 + 2 + 2;
   // tmem base (u32), abort flag (int), wait limit (u64, ns)
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kBytes = kOffMisc + 16;
@@ -266,6 +266,10 @@ __global__ void __launch_bounds__(512, 1)
   };
   using L = FwdLayout<DP, MODE>;
   constexpr int SQ = L::kStagesQ, SK = L::kStagesK, SV = L::kStagesV;
+  // P(j) is handed to the PV issuers in PH parts per group (d = 128: two halves of 32 keys, so
+  // the first half's MMAs go in while the second half's exponentials run; d = 64, where the
+  // softmax itself is the limit, in one part)
+  constexpr int PH = DP == 128 ? 2 : 1;
   constexpr int kChunks = DP / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // The 128-byte swizzle atoms need 1024-byte aligned tiles and the layout has no slack to
@@ -287,12 +291,13 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* k_empty = k_full + SK;
   uint64_t* v_full = k_empty + SK;
   uint64_t* v_empty = v_full + SV;
-  // Per buffer b: s_full (S(j) ready), p_full[b * 2 + g] (group g has written P(j)), pv_done
+  // Per buffer b: s_full (S(j) ready), p_full[b * 4 + g * 2 + h] (group g has written keys
+  // [32h, 32h + 32) of its half of P(j)), pv_done
   // (PV(j) of both groups done: one commit from each PV issuer), for the tiles j with
   // j % 2 == b; phase k is tile 2k + b.
   uint64_t* s_full = v_empty + SV;
   uint64_t* p_full = s_full + 2;
-  uint64_t* pv_done = p_full + 4;
+  uint64_t* pv_done = p_full + 8;
   uint64_t* o_free = pv_done + 2;
   uint64_t* drain = o_free + 1;
   uint64_t* o_staged = drain + 1;  // [Q slot]: the softmax warps have staged a tile-stored item's O
@@ -320,8 +325,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + 2 * i, 4);  // one arrival per softmax warp of the group
-      mbar_init(p_full + 2 * i + 1, 4);
+      for (int h = 0; h < 4; ++h) mbar_init(p_full + 4 * i + h, 4);  // one arrival per softmax warp of the group
       mbar_init(pv_done + i, 2);
     }
     mbar_init(o_free, 4);  // one arrival per epilogue warp
@@ -503,14 +507,21 @@ __global__ void __launch_bounds__(512, 1)
               const uint64_t vx = dV + (((t % SV) * L::kTileBytes) >> 4);
               const uint32_t acc0 = j == 0 ? 0u : 1u;
               // PV_g(t): O_g (+)= P_g(t) V[64g, 64g + 64), P_g over the first 32 columns of group
-              // g's half of S buffer b (keys 2c, 2c+1 in column c)
-              if (!mbar_wait(p_full + 2 * b + g, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-              tc_fence_after();
+              // g's half of S buffer b (keys 2c, 2c+1 in column c), each of its PH parts issued as
+              // soon as the softmax has written it
               const uint32_t pa = tmem + b * 128 + g * 64;
               const uint64_t vg = vx + ((g * 4 * 2048) >> 4);
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                mma_ts(tmem + L::kColO + g * DP, pa + ks * 8, vg + ((ks * 2048) >> 4), idO, ks > 0 ? 1u : acc0);
+              for (int h = 0; h < PH; ++h) {
+                if (!mbar_wait(p_full + 4 * b + 2 * g + h, (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int k2 = 0; k2 < 4 / PH; ++k2) {
+                  const int ks = (4 / PH) * h + k2;
+                  mma_ts(tmem + L::kColO + g * DP, pa + ks * 8, vg + ((ks * 2048) >> 4), idO, ks > 0 ? 1u : acc0);
+                }
+              }
+              if (!ok) break;
               mma_commit(pv_done + b);
               mma_commit(v_empty + t % SV);
             }
@@ -737,48 +748,15 @@ __global__ void __launch_bounds__(512, 1)
           m = mx2;
         }
         const float mb = (m == -INFINITY) ? 0.f : m;
-        // exponentials in pairs: x = s * scale * log2(e) - m with one paired FMA, 2^x, the row
-        // sum in 4 paired chains, and the 16-bit pair of P.  In tiles with no masked key the
-        // pairs selected by kPolyPairs run on the FMA pipe, the rest on the special-function
-        // unit; masked tiles use the latter only (exact zeros).
-        const uint64_t scl = f2_pack(sl2, sl2), nmb = f2_pack(-mb, -mb);
-        uint64_t acc[4];
-        uint32_t pk[32];
-        if (lim >= 63) {
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const uint64_t x = f2_fma(f2_pack(s[c], s[c + 1]), scl, nmb);
-            uint64_t e;
-            if ((kPolyPairs >> ((c >> 1) & 7)) & 1) {
-              e = exp2_fma2(x);
-            } else {
-              const float2 xf = f2_unpack(x);
-              e = f2_pack(ex2_approx(xf.x), ex2_approx(xf.y));
-            }
-            acc[(c >> 1) & 3] = c < 8 ? e : f2_add(acc[(c >> 1) & 3], e);
-            const float2 ef = f2_unpack(e);
-            pk[c / 2] = Elem<T>::pack(ef.x, ef.y);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float2 xf = f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), scl, nmb));
-            const float e0 = ex2_approx(xf.x), e1 = ex2_approx(xf.y);
-            const uint64_t e = f2_pack(e0, e1);
-            acc[(c >> 1) & 3] = c < 8 ? e : f2_add(acc[(c >> 1) & 3], e);
-            pk[c / 2] = Elem<T>::pack(e0, e1);
-          }
-        }
-        const float2 rs2 = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
-        l = l * alpha + (rs2.x + rs2.y);
-        // P over the first 32 of this group's S columns, already in registers; the S buffer takes
-        // S(t+2) only after PV(t) has read P
-        tmem_st32(tS, pk);
-        // O_g *= alpha: O_g must hold PV(t-1) first, so wait for it (only when rescaling)
-        if (__any_sync(0xffffffffu, resc)) {
+        // O_g *= alpha (only when rescaling): O_g must hold PV(t-1) first, so wait for it.  Done
+        // before the first part of P(t) is handed over: ahead of the exponentials when P goes
+        // in two parts, after P's store when it goes in one.
+        bool resc_ok = true;
+        auto rescale_o = [&]() {
+          if (!__any_sync(0xffffffffu, resc)) return;
           if (t > 0 && !mbar_wait_warp(pv_done + ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
+            resc_ok = false;
+            return;
           }
           tc_fence_after();
           const float a = resc ? alpha : 1.f;
@@ -792,10 +770,67 @@ __global__ void __launch_bounds__(512, 1)
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
             tmem_st32(tOg + c * 32, r);
           }
+        };
+        if constexpr (PH == 2) rescale_o();
+        if (!resc_ok) {
+          ok = false;
+          break;
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive_warp(p_full + 2 * b + grp);
+        // exponentials in pairs: x = s * scale * log2(e) - m with one paired FMA, 2^x, the row
+        // sum in 4 paired chains, and the 16-bit pair of P.  In tiles with no masked key the
+        // pairs selected by kPolyPairs run on the FMA pipe, the rest on the special-function
+        // unit; masked tiles use the latter only (exact zeros).
+        const uint64_t scl = f2_pack(sl2, sl2), nmb = f2_pack(-mb, -mb);
+        uint64_t acc[4];
+        // P over the first 32 of this group's S columns, in PH parts of 64 / PH keys: each part
+        // is stored and handed to its PV issuer while the next part's exponentials run.  The S
+        // buffer takes S(t+2) only after PV(t) has read P.
+        constexpr int PK = 64 / PH;  // keys per part
+#pragma unroll
+        for (int h = 0; h < PH; ++h) {
+          uint32_t pk[PK / 2];
+          if (lim >= 63) {
+#pragma unroll
+            for (int c = PK * h; c < PK * h + PK; c += 2) {
+              const uint64_t x = f2_fma(f2_pack(s[c], s[c + 1]), scl, nmb);
+              uint64_t e;
+              if ((kPolyPairs >> ((c >> 1) & 7)) & 1) {
+                e = exp2_fma2(x);
+              } else {
+                const float2 xf = f2_unpack(x);
+                e = f2_pack(ex2_approx(xf.x), ex2_approx(xf.y));
+              }
+              acc[(c >> 1) & 3] = c < 8 ? e : f2_add(acc[(c >> 1) & 3], e);
+              const float2 ef = f2_unpack(e);
+              pk[(c / 2) % (PK / 2)] = Elem<T>::pack(ef.x, ef.y);
+            }
+          } else {
+#pragma unroll
+            for (int c = PK * h; c < PK * h + PK; c += 2) {
+              const float2 xf = f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), scl, nmb));
+              const float e0 = ex2_approx(xf.x), e1 = ex2_approx(xf.y);
+              const uint64_t e = f2_pack(e0, e1);
+              acc[(c >> 1) & 3] = c < 8 ? e : f2_add(acc[(c >> 1) & 3], e);
+              pk[(c / 2) % (PK / 2)] = Elem<T>::pack(e0, e1);
+            }
+          }
+          if constexpr (PH == 2) {
+            tmem_st16(tS + 16 * h, pk);
+          } else {
+            tmem_st32(tS, pk);
+            rescale_o();
+            if (!resc_ok) break;
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive_warp(p_full + 4 * b + 2 * grp + h);
+        }
+        if (!resc_ok) {
+          ok = false;
+          break;
+        }
+        const float2 rs2 = f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])));
+        l = l * alpha + (rs2.x + rs2.y);
       }
       if (!ok) break;
       kv += it.n_kv;
