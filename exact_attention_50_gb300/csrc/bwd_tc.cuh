@@ -54,9 +54,9 @@ struct BwdLayout {
   static constexpr int kOffRow = kOffStage + kOwnStageChunks * kChunkBytes;  // LSE*log2e and D, 2 buffers each
   static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
   // kv_full, q_full[QS], q_empty[QS], do_full[QS], do_empty[QS], s_full, dp_full, p_full,
-  // dv_done, ds_full, dsl_free, stage_free, dq_full, dq_free, dkdv_done, rows_ready,
+  // dv_done, ds_full[2], dsl_free, stage_free, dq_full, dq_free, dkdv_done, rows_ready,
   // stage_full, drain, drain2
-  static constexpr int kNumBars = 1 + 4 * kQStages + 14;
+  static constexpr int kNumBars = 1 + 4 * kQStages + 15;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag, wait limit (u64)
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
@@ -132,9 +132,11 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* dp_full = s_full + 1;
   uint64_t* p_full = dp_full + 1;
   uint64_t* dv_done = p_full + 1;
+  // ds_full[h]: every elementwise warp has written dS^T for the first (h = 0) or last (h = 1) 32
+  // of its 64 query columns, i.e. the dK k-steps {0, 1, 4, 5} or {2, 3, 6, 7}
   uint64_t* ds_full = dv_done + 1;
   // the dS lo area also stages dQ columns 64-127: free once the tile's reduction has read it
-  uint64_t* dsl_free = ds_full + 1;
+  uint64_t* dsl_free = ds_full + 2;
   uint64_t* stage_free = dsl_free + 1;  // the reductions have read the own staging buffer
   uint64_t* dq_full = stage_free + 1;
   uint64_t* dq_free = dq_full + 1;
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(p_full, kEw / 32);  // one arrival per warp
     mbar_init(dv_done, 1);
     mbar_init(ds_full, kEw / 32);
+    mbar_init(ds_full + 1, kEw / 32);
     mbar_init(dsl_free, 1);
     mbar_init(stage_free, 1);
     mbar_init(dq_full, 1);
@@ -329,18 +332,25 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(do_empty + st);
         } else {
           // ---- dK += dS^T Q (hi, lo)
-          if (!mbar_wait(ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
+          // in two parts, each as soon as the elementwise warps have written its 64 queries:
+          // k-steps {0, 1, 4, 5} (the first 32 columns of each warp's half), then {2, 3, 6, 7}
           {
             const uint64_t ah = opaque(dSh_k), al = opaque(dSl_k), bq = opaque(dQ_mn + st * kStage16);
             const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks) {
-              const uint32_t a_off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
-              const uint64_t bd = bq + ((ks * 2048) >> 4);
-              mma_ss(tmem + L::kColdK, ah + a_off, bd, idKD, ks > 0 ? 1u : acc0);
-              mma_ss(tmem + L::kColdK, al + a_off, bd, idKD, 1u);
+            for (int h = 0; h < 2; ++h) {
+              if (!mbar_wait(ds_full + h, it & 1, abort_flag, p.status)) { ok = false; break; }
+              tc_fence_after();
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int ks = (j >> 1) * 4 + 2 * h + (j & 1);
+                const uint32_t a_off = ((ks >> 2) * L::kChunkBytes + (ks & 3) * 32) >> 4;
+                const uint64_t bd = bq + ((ks * 2048) >> 4);
+                mma_ss(tmem + L::kColdK, ah + a_off, bd, idKD, (h > 0 || j > 0) ? 1u : acc0);
+                mma_ss(tmem + L::kColdK, al + a_off, bd, idKD, 1u);
+              }
             }
+            if (!ok) break;
           }
           mma_commit(q_empty + st);
           // ---- dQ_t = dS K (hi, lo), dS read MN-major from the dS^T tiles, into the dP columns
@@ -386,13 +396,19 @@ __global__ void __launch_bounds__(512, 1)
       if (!mbar_wait_warp(dq_full, it & 1, abort_flag, p.status)) { ok = false; break; }
       if (it >= 1 && !mbar_wait_warp(stage_free, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll 1
+      // chunk c + 1 is loaded from TMEM while chunk c is written to its staging buffer, and the
+      // dQ columns are released (dq_free, which the next dP^T waits for) once the last is loaded
+      uint32_t ra[32], rb[32];
+      tmem_ld32(tl + L::kColdQ, ra);
+      tmem_ld_wait();
+      tmem_reg_fence(ra);
+#pragma unroll
       for (int c = 0; c < DP / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tl + L::kColdQ + c * 32, r);
-        tmem_ld_wait();
-        tmem_reg_fence(r);
-        if (c == DP / 32 - 1) {
+        uint32_t(&r)[32] = (c & 1) ? rb : ra;
+        uint32_t(&nx)[32] = (c & 1) ? ra : rb;
+        if (c + 1 < DP / 32) {
+          tmem_ld32(tl + L::kColdQ + (c + 1) * 32, nx);
+        } else {
           tc_fence_before();
           mbar_arrive_warp(dq_free);  // the dQ columns may be overwritten once everything is loaded
         }
@@ -400,6 +416,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int g = 0; g < 8; ++g)
           *reinterpret_cast<uint4*>(row + ((g ^ (t & 7)) << 4)) = make_uint4(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3]);
+        if (c + 1 < DP / 32) {
+          tmem_ld_wait();
+          tmem_reg_fence(nx);
+        }
       }
       fence_async_smem();
       mbar_arrive_warp(stage_full);
@@ -576,47 +596,58 @@ __global__ void __launch_bounds__(512, 1)
       // the dS hi area is free; the dS lo area waits for the reductions of the dQ chunks staged in it.
       if (!mbar_wait_warp(dp_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tl + L::kColdP + half * 64, r0);
-        tmem_ld32(tl + L::kColdP + half * 64 + 32, r1);
-        tmem_ld_wait();
-        tmem_reg_fence(r0);
-        tmem_reg_fence(r1);
-        // dS = P (dP - D), with D (stored negated) read as float4
-        const float4* nd4 = reinterpret_cast<const float4*>(d_buf + half * 64);
-#pragma unroll
-        for (int i4 = 0; i4 < 16; ++i4) {
-          const float4 nd = nd4[i4];
-          const int i = 4 * i4;
-          pv[i] *= __uint_as_float(i < 32 ? r0[i] : r1[i - 32]) + nd.x;
-          pv[i + 1] *= __uint_as_float(i < 32 ? r0[i + 1] : r1[i - 31]) + nd.y;
-          pv[i + 2] *= __uint_as_float(i < 32 ? r0[i + 2] : r1[i - 30]) + nd.z;
-          pv[i + 3] *= __uint_as_float(i < 32 ? r0[i + 3] : r1[i - 29]) + nd.w;
-        }
-      }
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tl + L::kColdP + half * 64, r0);
+      tmem_ld32(tl + L::kColdP + half * 64 + 32, r1);
+      tmem_ld_wait();
+      tmem_reg_fence(r0);
+      tmem_reg_fence(r1);
       tc_fence_before();  // the dP columns are consumed (the dQ MMA may overwrite them)
-      uint4 lo[8];
+      // dS = P (dP - D), with D (stored negated) read as float4, split hi/lo and written in two
+      // parts of 32 query columns, each handed over (ds_full[h]) as soon as it is in shared
+      // memory, so the first half of the dK MMAs goes in while the second part is computed
+      const float4* nd4 = reinterpret_cast<const float4*>(d_buf + half * 64);
+      bool stop = false;
 #pragma unroll
-      for (int gi = 0; gi < 8; ++gi) {
-        const int gq = half * 8 + gi;  // 16-byte granule index over the 128 queries
-        const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
-        uint4 a;
-        split_pack<T>(pv[gi * 8 + 0], pv[gi * 8 + 1], a.x, lo[gi].x);
-        split_pack<T>(pv[gi * 8 + 2], pv[gi * 8 + 3], a.y, lo[gi].y);
-        split_pack<T>(pv[gi * 8 + 4], pv[gi * 8 + 5], a.z, lo[gi].z);
-        split_pack<T>(pv[gi * 8 + 6], pv[gi * 8 + 7], a.w, lo[gi].w);
-        *reinterpret_cast<uint4*>(sdSh + off) = a;
-      }
-      if (L::kLoStageChunks > 0 && it >= 1 && !mbar_wait_warp(dsl_free, (it - 1) & 1, abort_flag, p.status)) break;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t(&r)[32] = h == 0 ? r0 : r1;
 #pragma unroll
-      for (int gi = 0; gi < 8; ++gi) {
-        const int gq = half * 8 + gi;
-        const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
-        *reinterpret_cast<uint4*>(sdSl + off) = lo[gi];
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 nd = nd4[8 * h + j4];
+          const int i = 32 * h + 4 * j4;
+          pv[i] *= __uint_as_float(r[4 * j4]) + nd.x;
+          pv[i + 1] *= __uint_as_float(r[4 * j4 + 1]) + nd.y;
+          pv[i + 2] *= __uint_as_float(r[4 * j4 + 2]) + nd.z;
+          pv[i + 3] *= __uint_as_float(r[4 * j4 + 3]) + nd.w;
+        }
+        uint4 lo[4];
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          const int gi = 4 * h + g4;
+          const int gq = half * 8 + gi;  // 16-byte granule index over the 128 queries
+          const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
+          uint4 a;
+          split_pack<T>(pv[gi * 8 + 0], pv[gi * 8 + 1], a.x, lo[g4].x);
+          split_pack<T>(pv[gi * 8 + 2], pv[gi * 8 + 3], a.y, lo[g4].y);
+          split_pack<T>(pv[gi * 8 + 4], pv[gi * 8 + 5], a.z, lo[g4].z);
+          split_pack<T>(pv[gi * 8 + 6], pv[gi * 8 + 7], a.w, lo[g4].w);
+          *reinterpret_cast<uint4*>(sdSh + off) = a;
+        }
+        if (h == 0 && L::kLoStageChunks > 0 && it >= 1 &&
+            !mbar_wait_warp(dsl_free, (it - 1) & 1, abort_flag, p.status)) {
+          stop = true;
+          break;
+        }
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          const int gq = half * 8 + 4 * h + g4;
+          const uint32_t off = (gq >> 3) * L::kChunkBytes + t * 128 + ((((gq & 7) ^ (t & 7))) << 4);
+          *reinterpret_cast<uint4*>(sdSl + off) = lo[g4];
+        }
+        fence_async_smem();
+        mbar_arrive_warp(ds_full + h);
       }
-      fence_async_smem();
-      mbar_arrive_warp(ds_full);
+      if (stop) break;
     }
   }
 
