@@ -53,10 +53,10 @@ struct BwdLayout {
   static constexpr int kOffStage = kOffdSl + 2 * kChunkBytes;
   static constexpr int kOffRow = kOffStage + kOwnStageChunks * kChunkBytes;  // LSE*log2e and D, 2 buffers each
   static constexpr int kOffBar = kOffRow + 4 * 128 * 4;
-  // kv_full, q_full[QS], q_empty[QS], do_full[QS], do_empty[QS], s_full, dp_full, p_full,
+  // kv_full, q_full[QS], q_empty[QS], do_full[QS], do_empty[QS], s_full, dp_full, p_full[2],
   // dv_done, ds_full[2], dsl_free, stage_free, dq_full, dq_free, dkdv_done, rows_ready,
   // stage_full, drain, drain2
-  static constexpr int kNumBars = 1 + 4 * kQStages + 15;
+  static constexpr int kNumBars = 1 + 4 * kQStages + 16;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag, wait limit (u64)
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kBytes;  // the dynamic shared memory starts 1024-byte aligned
@@ -130,8 +130,10 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* do_empty = do_full + QS;
   uint64_t* s_full = do_empty + QS;
   uint64_t* dp_full = s_full + 1;
+  // p_full[h]: every elementwise warp has written P^T for the first (h = 0) or last (h = 1) 32 of
+  // its 64 query columns, i.e. the dV k-steps {0, 1, 4, 5} or {2, 3, 6, 7}
   uint64_t* p_full = dp_full + 1;
-  uint64_t* dv_done = p_full + 1;
+  uint64_t* dv_done = p_full + 2;
   // ds_full[h]: every elementwise warp has written dS^T for the first (h = 0) or last (h = 1) 32
   // of its 64 query columns, i.e. the dK k-steps {0, 1, 4, 5} or {2, 3, 6, 7}
   uint64_t* ds_full = dv_done + 1;
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_full, kEw / 32);  // one arrival per warp
+    mbar_init(p_full + 1, kEw / 32);
     mbar_init(dv_done, 1);
     mbar_init(ds_full, kEw / 32);
     mbar_init(ds_full + 1, kEw / 32);
@@ -315,18 +318,25 @@ __global__ void __launch_bounds__(512, 1)
           mma_commit(dp_full);
           // ---- dV += P^T dO; P^T hi/lo in TMEM: the 16 queries of k-step ks sit in the 32-column
           // group ks/2 (hi in its first 16 columns, lo in the last 16), 8 columns per k-step
-          if (!mbar_wait(p_full, it & 1, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
+          // in two parts, each as soon as the elementwise warps have written it: k-steps
+          // {0, 1, 4, 5} (the first 32 columns of each warp's half), then {2, 3, 6, 7}
           {
             const uint64_t bo = opaque(ddO_mn + st * kStage16);
             const uint32_t acc0 = it > 0 ? 1u : 0u;
 #pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks) {
-              const uint32_t acol = L::kColS + (ks >> 1) * 32 + (ks & 1) * 8;
-              const uint64_t bd = bo + ((ks * 2048) >> 4);
-              mma_ts(tmem + L::kColdV, tmem + acol, bd, idKD, ks > 0 ? 1u : acc0);
-              mma_ts(tmem + L::kColdV, tmem + acol + 16, bd, idKD, 1u);
+            for (int h = 0; h < 2; ++h) {
+              if (!mbar_wait(p_full + h, it & 1, abort_flag, p.status)) { ok = false; break; }
+              tc_fence_after();
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int ks = (j >> 1) * 4 + 2 * h + (j & 1);
+                const uint32_t acol = L::kColS + (ks >> 1) * 32 + (ks & 1) * 8;
+                const uint64_t bd = bo + ((ks * 2048) >> 4);
+                mma_ts(tmem + L::kColdV, tmem + acol, bd, idKD, (h > 0 || j > 0) ? 1u : acc0);
+                mma_ts(tmem + L::kColdV, tmem + acol + 16, bd, idKD, 1u);
+              }
             }
+            if (!ok) break;
           }
           mma_commit(dv_done);
           mma_commit(do_empty + st);
@@ -511,8 +521,8 @@ __global__ void __launch_bounds__(512, 1)
     const int key = kt * kBN + t;
     const bool key_ok = key < kv_len;
     const float sl2 = p.scale_log2;
-    // The next tile's row terms are loaded one tile ahead and used only when they are written to
-    // shared memory at the start of that tile, so no thread waits for the loads in between.
+    // The next tile's row terms are loaded at the end of the current tile and used only when they
+    // are written to shared memory at the start of the next one, ahead of the wait for its S^T.
     // Rows past the sequence read its last row and are replaced there.
     float lse_next = 0.f, d_next = 0.f;
     bool row_next = false;
@@ -551,46 +561,46 @@ __global__ void __launch_bounds__(512, 1)
         tmem_reg_fence(r0);
         tmem_reg_fence(r1);
         // P = 2^(S scale log2e - LSE log2e): the row terms as float4 from shared memory, the
-        // argument as one paired FMA per two queries
+        // argument as one paired FMA per two queries.  In two parts of 32 query columns, each
+        // written back to TMEM and handed over (p_full[cc]) before the next is computed, so the
+        // first half of the dV MMAs runs while the second part is computed.
         const float4* nl4 = reinterpret_cast<const float4*>(lse_buf + half * 64);
         const uint64_t scl = f2_pack(sl2, sl2);
-#pragma unroll
-        for (int i4 = 0; i4 < 16; ++i4) {
-          const float4 nl = nl4[i4];
-          const int i = 4 * i4;
-          const float s0 = __uint_as_float(i < 32 ? r0[i] : r1[i - 32]);
-          const float s1 = __uint_as_float(i < 32 ? r0[i + 1] : r1[i - 31]);
-          const float s2 = __uint_as_float(i < 32 ? r0[i + 2] : r1[i - 30]);
-          const float s3 = __uint_as_float(i < 32 ? r0[i + 3] : r1[i - 29]);
-          const float2 x01 = f2_unpack(f2_fma(f2_pack(s0, s1), scl, f2_pack(nl.x, nl.y)));
-          const float2 x23 = f2_unpack(f2_fma(f2_pack(s2, s3), scl, f2_pack(nl.z, nl.w)));
-          pv[i] = ex2_approx(x01.x);
-          pv[i + 1] = ex2_approx(x01.y);
-          pv[i + 2] = ex2_approx(x23.x);
-          pv[i + 3] = ex2_approx(x23.y);
-        }
         // queries q < key - off are masked under causal (only tiles on the diagonal have any; a
         // query row that sees no key at all has every column masked), and keys past the
         // sequence give P = 0: the selects run only where a thread has such columns
         // columns c < lim are masked (a key past the sequence: all 64)
         const int lim = !key_ok ? 64 : (CAUSAL ? key - off - qt * kBM - half * 64 : -1);
-        if (lim > 0) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) pv[i] = i < lim ? 0.f : pv[i];
-        }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
+          uint32_t(&r)[32] = cc == 0 ? r0 : r1;
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 nl = nl4[8 * cc + j4];
+            const int i = 32 * cc + 4 * j4;
+            const float2 x01 = f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * j4]), __uint_as_float(r[4 * j4 + 1])), scl,
+                                                f2_pack(nl.x, nl.y)));
+            const float2 x23 = f2_unpack(f2_fma(f2_pack(__uint_as_float(r[4 * j4 + 2]), __uint_as_float(r[4 * j4 + 3])),
+                                                scl, f2_pack(nl.z, nl.w)));
+            pv[i] = ex2_approx(x01.x);
+            pv[i + 1] = ex2_approx(x01.y);
+            pv[i + 2] = ex2_approx(x23.x);
+            pv[i + 3] = ex2_approx(x23.y);
+          }
+          if (lim > 32 * cc) {
+#pragma unroll
+            for (int i = 32 * cc; i < 32 * cc + 32; ++i) pv[i] = i < lim ? 0.f : pv[i];
+          }
           uint32_t ph[16], pl[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) split_pack<T>(pv[cc * 32 + 2 * i], pv[cc * 32 + 2 * i + 1], ph[i], pl[i]);
           tmem_st16(tl + L::kColS + half * 64 + cc * 32, ph);
           tmem_st16(tl + L::kColS + half * 64 + cc * 32 + 16, pl);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive_warp(p_full + cc);
         }
-        tmem_st_wait();
       }
-      tc_fence_before();
-      mbar_arrive_warp(p_full);
-      load_rows(it + 1);  // prefetch the next tile's LSE and D
       // ---- phase 2: dS^T = P^T (dP^T - D), hi/lo into shared memory.  dp_full also means the
       // previous tile's dK and dQ MMAs have completed (dP^T is issued after its dQ read-out), so
       // the dS hi area is free; the dS lo area waits for the reductions of the dQ chunks staged in it.
@@ -648,6 +658,8 @@ __global__ void __launch_bounds__(512, 1)
         mbar_arrive_warp(ds_full + h);
       }
       if (stop) break;
+      // the next tile's LSE and D: their latency passes while this warp waits for the next S^T
+      load_rows(it + 1);
     }
   }
 
