@@ -22,7 +22,9 @@
 // 512 threads, four warpgroups with a register split:
 //   WG0, WG1  elementwise (two warps per TMEM lane quadrant, each on half of the 128 query
 //             columns): phase 1 turns S^T into P^T (hi/lo, back into TMEM), phase 2 turns dP^T
-//             into dS^T (hi/lo, into shared memory).  The next tile's LSE and D are prefetched.
+//             into dS^T (hi/lo, into shared memory), each in two parts of 32 columns handed
+//             over separately so the dV / dK MMAs on the first part start early.  The next
+//             tile's LSE and D are prefetched.
 //   WG2       moves dQ_t from TMEM through shared memory into the fp32 workspace (TMA tile
 //             reductions; in key-tile order when deterministic) and writes dK, dV at the end.
 //   WG3       warp 12: TMA producer and TMEM allocator; warps 13 and 14: MMA issuers.
