@@ -69,3 +69,37 @@ def test_fp32_alu_peak_derivation():
     import bench
     # 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz
     assert bench.fp32_alu_peak(152, 2070.0) == pytest.approx(80.55, rel=1e-3)
+
+
+def test_committed_traffic_only_for_the_measured_code(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu figure only while the device code carries
+    the stamp it was measured on; any other stamp, a missing entry or a missing file gives null."""
+    import json
+    import bench
+    stamp = bench.source_stamp()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    entry = {"bwd_tc_kernel": {"gqa_bf16": {"dram_bytes_per_launch": 123456, "source_stamp": stamp}},
+             "fwd_tc_kernel": {"gqa_bf16": {"dram_bytes_per_launch": 7, "source_stamp": "0" * 64}}}
+    (prof / "ncu_traffic.json").write_text(json.dumps(entry))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.committed_traffic("bwd_tc_kernel", "gqa_bf16") == 123456
+    assert bench.committed_traffic("fwd_tc_kernel", "gqa_bf16") is None  # measured on other code
+    assert bench.committed_traffic("fwd_tc_kernel", "decode_bf16") is None  # no entry
+    (prof / "ncu_traffic.json").unlink()
+    assert bench.committed_traffic("bwd_tc_kernel", "gqa_bf16") is None  # no file
+
+
+def test_code_stamp_ignores_comments_but_not_code():
+    """The stamp follows the device code only: a comment edit keeps it, a code edit changes it."""
+    from exact_attention_50_gb300 import build
+    base = build.code_stamp()
+
+    def read_with(edit):
+        def read(path):
+            text = open(path).read()
+            return edit(text) if path.endswith("fwd_tc.cuh") else text
+        return read
+
+    assert build.code_stamp(read_with(lambda t: t + "\n// a comment only\n")) == base
+    assert build.code_stamp(read_with(lambda t: t.replace("kRescaleLog2 = 8.0f", "kRescaleLog2 = 7.0f"))) != base
