@@ -96,7 +96,7 @@ struct FwdLayout {
   static constexpr int kOffBar = kOffX + 2 * 2 * 128 * 4;
   // q_full[2], q_empty[2], k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], s_full[2],
   // p_full[2 buffers][2 groups][2 halves], pv_done[2], o_free, drain,
-  // o_staged[2] (per Q slot, so it cannot run two phases ahead of the store warp: a slot takes
+  // o_staged[2] (per Q slot, so it cannot run two phases ahead of the tile stores: a slot takes
   // a new Q only after the tile staged in it has been written out), drain2, drain3,
   // stats_ready, stats_free
   static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 2 + 8 + 2 + 1 + 1 + 2 + 2 + 2;
@@ -255,11 +255,11 @@ __global__ void __launch_bounds__(512, 1)
   constexpr bool VARLEN = MODE == kModeVarlen;
   constexpr bool KV = MODE == kModeKv;
   // 16-bit output of a dense item, or of a varlen item whose 128 rows all lie in its
-  // sequence: the softmax warps stage the item's O tile in the item's Q slot (free once its
-  // last S has run) and warp 10 writes it with tile stores, then frees the slot.  Otherwise (a
-  // varlen tile that ends past its sequence must not write into the next one; fp32 output or
-  // KV-cache partials) the softmax warps store their rows themselves and the last S frees the
-  // Q slot.  Every role decides per item with the same function.
+  // sequence: the epilogue warps stage the item's O tile in the item's Q slot (free once its
+  // last S has run) and their thread 0 writes it with tile stores, then frees the slot.
+  // Otherwise (a varlen tile that ends past its sequence must not write into the next one; fp32
+  // output or KV-cache partials) the epilogue warps store their rows themselves and the last S
+  // frees the Q slot.  Every role decides per item with the same function.
   const bool tile_out = (MODE == kModeDense || MODE == kModeVarlen) && !p.out_f32;
   auto tile_item = [&](const FwdItem& it) -> bool {
     return tile_out && (MODE == kModeDense || (it.qt + 1) * kBM <= it.seq_len);
@@ -543,7 +543,8 @@ __global__ void __launch_bounds__(512, 1)
     // Per item, thread t (row t): both groups' (max, sum) from the softmax warps, then, once the
     // item's last PV has completed, O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l over the whole
     // row, released from TMEM as soon as it is loaded (o_free), and LSE = m + ln l.  16-bit
-    // tiles are staged in the item's Q slot for the store warp; otherwise rows are stored here.
+    // tiles are staged in the item's Q slot and written out by this warpgroup's thread 0 with
+    // tile stores; otherwise rows are stored here.
     const int row = threadIdx.x - 384;  // TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const bool storer = row == 0 && tile_out;  // issues the tile stores of staged items
